@@ -1,0 +1,248 @@
+"""Seeded synthetic inputs shared by the tests, the smoke run and the benchmark.
+
+This module only draws random data and lays it out in the formats the DCP entry points
+take; it computes nothing the method computes.  Both the float64 oracle and the CUDA path
+consume what it returns.
+
+Recipe (shapes follow the pages' workloads; values are synthetic):
+
+* Q: ``[B][T][H][576]`` BF16, N(0, 1) rounded to nearest-even.
+* KV pools: one per DCP rank, ``[slots][64][576]``; BF16 N(0, 1), or FP8-E4M3 of N(0, 1)
+  divided by a per-tensor scale ``kv_scale = 8 / 448`` (the E4M3 range then covers +-8
+  sigma; values are clamped there before the round-to-nearest-even cast).
+* Page table: logical page ``j`` of request ``b`` is owned by rank ``j mod N`` (round-robin
+  ownership) and sits in a seeded uniformly random free slot of that rank's pool; the table
+  stores the decode-side global page value ``slot * N + owner``.
+* Sequence lengths: given per config; the last page of a request may be partly filled, and
+  its tail rows hold finite random data like every other row.
+* Source (prefill, CP layer-split) pools: ``[layers owned][pages][64][576]`` with random
+  content; each request's source pages are contiguous or a seeded random permutation.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import torch
+
+PAGE = 64
+K_DIM = 576
+V_DIM = 512
+FP8_KV_SCALE = 8.0 / 448.0
+SOFTMAX_SCALE = 1.0 / math.sqrt(192.0)
+
+
+def _gen(seed: int, device) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    return g
+
+
+def _randn_into(out: torch.Tensor, gen: torch.Generator, scale: float | None,
+                chunk: int = 1 << 27) -> None:
+    """Fill ``out`` (bf16 or float8_e4m3fn) with N(0,1) values (divided by ``scale`` for fp8)."""
+    flat = out.view(-1)
+    for s in range(0, flat.numel(), chunk):
+        n = min(chunk, flat.numel() - s)
+        x = torch.randn(n, generator=gen, device=out.device, dtype=torch.float32)
+        if out.dtype == torch.float8_e4m3fn:
+            x = (x / scale).clamp_(-448.0, 448.0)
+        flat[s:s + n] = x.to(out.dtype)
+
+
+def kv_dtype(name: str) -> torch.dtype:
+    return {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}[name]
+
+
+def random_pool(n_slots: int, dtype: str, gen: torch.Generator, device, layers: int = 0) -> torch.Tensor:
+    shape = (n_slots, PAGE, K_DIM) if layers == 0 else (layers, n_slots, PAGE, K_DIM)
+    t = torch.empty(shape, dtype=kv_dtype(dtype), device=device)
+    _randn_into(t, gen, FP8_KV_SCALE)
+    return t
+
+
+def random_q(b: int, t: int, h: int, gen: torch.Generator, device) -> torch.Tensor:
+    q = torch.empty((b, t, h, K_DIM), dtype=torch.bfloat16, device=device)
+    _randn_into(q, gen, None)
+    return q
+
+
+def page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Generator):
+    """Round-robin ownership with seeded random slots.  Returns (req_page_ptr, dst_vpages)."""
+    pages = [(int(n) + PAGE - 1) // PAGE for n in seq_lens]
+    ptr = [0]
+    for p in pages:
+        ptr.append(ptr[-1] + p)
+    n_ranks = max(n_dcp, 1)
+    perms = [torch.randperm(slots_per_rank, generator=gen, device="cpu") for _ in range(n_ranks)]
+    used = [0] * n_ranks
+    vp = torch.empty(ptr[-1], dtype=torch.int64)
+    k = 0
+    for p in pages:
+        j = torch.arange(p)
+        owner = j % n_ranks
+        for d in range(n_ranks):
+            sel = owner == d
+            cnt = int(sel.sum())
+            if used[d] + cnt > slots_per_rank:
+                raise ValueError("pool too small for the page table")
+            slots = perms[d][used[d]:used[d] + cnt]
+            used[d] += cnt
+            vp[k:k + p][sel] = slots * n_ranks + d if n_dcp > 1 else slots
+        k += p
+    return torch.tensor(ptr, dtype=torch.int64), vp.to(torch.int32)
+
+
+@dataclass
+class AttnCase:
+    """One partial-attention workload (all tensors on ``device``)."""
+    B: int
+    T: int
+    H: int
+    n_dcp: int
+    dtype: str
+    seq_lens: torch.Tensor          # int32 [B]
+    req_page_ptr: torch.Tensor      # int64 [B+1]
+    dst_vpages: torch.Tensor        # int32 [pages]
+    q: torch.Tensor                 # bf16 [B][T][H][576]
+    pools: list                     # per rank [slots][64][576]
+    slots_per_rank: int
+    kv_scale: float
+    softmax_scale: float = SOFTMAX_SCALE
+    name: str = ""
+
+    @property
+    def rows(self) -> int:
+        return self.B * self.T * self.H
+
+    @property
+    def max_tokens(self) -> int:
+        return int(self.seq_lens.max().item()) if self.B else 0
+
+
+def attention_case(seq_lens, H: int, T: int, n_dcp: int, dtype: str, slots_per_rank: int | None,
+                   seed: int, device, name: str = "") -> AttnCase:
+    gen_cpu = _gen(seed, "cpu")
+    gen_dev = _gen(seed + 1000003, device)
+    seq_lens = [int(n) for n in seq_lens]
+    n_ranks = max(n_dcp, 1)
+    per_rank = [0] * n_ranks
+    for n in seq_lens:
+        p = (n + PAGE - 1) // PAGE
+        for d in range(n_ranks):
+            per_rank[d] += (p - d + n_ranks - 1) // n_ranks if p > d else 0
+    need = max(per_rank) if per_rank else 0
+    if slots_per_rank is None:
+        slots_per_rank = max(need, 1)
+    ptr, vp = page_table(seq_lens, n_dcp, slots_per_rank, gen_cpu)
+    q = random_q(len(seq_lens), T, H, gen_dev, device)
+    pools = [random_pool(slots_per_rank, dtype, gen_dev, device) for _ in range(n_ranks)]
+    return AttnCase(B=len(seq_lens), T=T, H=H, n_dcp=n_dcp, dtype=dtype,
+                    seq_lens=torch.tensor(seq_lens, dtype=torch.int32, device=device),
+                    req_page_ptr=ptr.to(device), dst_vpages=vp.to(device), q=q, pools=pools,
+                    slots_per_rank=slots_per_rank,
+                    kv_scale=FP8_KV_SCALE if dtype == "e4m3" else 1.0, name=name)
+
+
+@dataclass
+class ReshardCase:
+    """A CP layer-split -> DCP page-interleaved reshard workload."""
+    n_layers: int
+    n_cp: int
+    n_dcp: int
+    dtype: str
+    seq_lens: list
+    req_page_ptr: torch.Tensor      # int64 [B+1]
+    src_pages: torch.Tensor         # int32 [pages]  prefill-side page index
+    dst_vpages: torch.Tensor        # int32 [pages]  decode-side global page value
+    src_pools: list                 # per CP rank [layers owned][src_pool_pages][64][576]
+    src_pool_pages: int
+    dst_pools: list                 # per DCP rank [n_layers][slots][64][576]
+    dst_slots: int
+    layer_counts: list = field(default_factory=list)
+    name: str = ""
+
+    @property
+    def page_bytes(self) -> int:
+        return PAGE * K_DIM * (2 if self.dtype == "bf16" else 1)
+
+
+SENTINEL_BYTE = 0xA5
+
+
+def reshard_case(seq_lens, n_layers: int, layer_counts: list, n_dcp: int, dtype: str,
+                 contiguous_src: bool, seed: int, device, dst_slots: int | None = None,
+                 src_pool_pages: int | None = None, name: str = "") -> ReshardCase:
+    """``layer_counts[r]`` = layers held by source rank r (the layer split itself is the
+    caller's; the generator only sizes the pools).  Destination pools are filled with the
+    sentinel byte so stray or missing writes show."""
+    gen_cpu = _gen(seed, "cpu")
+    gen_dev = _gen(seed + 1000003, device)
+    pages = [(int(n) + PAGE - 1) // PAGE for n in seq_lens]
+    total = sum(pages)
+    n_ranks = max(n_dcp, 1)
+    per_rank = [0] * n_ranks
+    for p in pages:
+        for d in range(n_ranks):
+            per_rank[d] += (p - d + n_ranks - 1) // n_ranks if p > d else 0
+    if dst_slots is None:
+        dst_slots = max(max(per_rank), 1)
+    ptr, vp = page_table(seq_lens, n_dcp, dst_slots, gen_cpu)
+    if src_pool_pages is None:
+        src_pool_pages = max(total, 1)
+    if contiguous_src:
+        src = torch.arange(total, dtype=torch.int32)
+    else:
+        src = torch.randperm(src_pool_pages, generator=gen_cpu)[:total].to(torch.int32)
+    src_pools = [random_pool(src_pool_pages, dtype, gen_dev, device, layers=c) for c in layer_counts]
+    dst_pools = []
+    for _ in range(n_ranks):
+        t = torch.empty((n_layers, dst_slots, PAGE, K_DIM), dtype=kv_dtype(dtype), device=device)
+        t.view(torch.uint8).fill_(SENTINEL_BYTE)
+        dst_pools.append(t)
+    return ReshardCase(n_layers=n_layers, n_cp=len(layer_counts), n_dcp=n_dcp, dtype=dtype,
+                       seq_lens=list(seq_lens), req_page_ptr=ptr.to(device),
+                       src_pages=src.to(device), dst_vpages=vp.to(device), src_pools=src_pools,
+                       src_pool_pages=src_pool_pages, dst_pools=dst_pools, dst_slots=dst_slots,
+                       layer_counts=list(layer_counts), name=name)
+
+
+def log_uniform_lengths(count: int, lo: int, hi: int, seed: int) -> list:
+    """Lengths exp(U[ln lo, ln hi]) rounded to a multiple of 64 (at least 64)."""
+    g = _gen(seed, "cpu")
+    u = torch.rand(count, generator=g, dtype=torch.float64)
+    x = torch.exp(math.log(lo) + u * (math.log(hi) - math.log(lo)))
+    return [max(PAGE, int(round(float(v) / PAGE)) * PAGE) for v in x]
+
+
+# The five workloads, by what they are.
+def tiny_case(device, seed: int = 0) -> AttnCase:
+    """1 request x 1024 tokens (16 pages), 16 heads, q_len 1, BF16, DCP=4."""
+    return attention_case([1024], H=16, T=1, n_dcp=4, dtype="bf16", slots_per_rank=4,
+                          seed=seed, device=device, name="tiny-1x1024-h16-bf16-dcp4")
+
+
+def batch_case(device, seed: int = 1) -> AttnCase:
+    """32 requests x 8192 tokens, 64 heads, q_len 1, BF16, DCP=8, 512 slots per rank."""
+    return attention_case([8192] * 32, H=64, T=1, n_dcp=8, dtype="bf16", slots_per_rank=512,
+                          seed=seed, device=device, name="batch-32x8192-h64-bf16-dcp8")
+
+
+def agent_case(device, seed: int = 2) -> AttnCase:
+    """48 requests x 100,000 tokens, 64 heads, q_len 1, FP8, DCP=8 over a ~2.8 GB pool."""
+    return attention_case([100_000] * 48, H=64, T=1, n_dcp=8, dtype="e4m3", slots_per_rank=9408,
+                          seed=seed, device=device, name="agent-48x100000-h64-fp8-dcp8")
+
+
+def long_eagle_case(device, seed: int = 3) -> AttnCase:
+    """4 requests x 1,048,576 tokens, 64 heads, q_len 4 (causal), FP8, DCP=8."""
+    return attention_case([1 << 20] * 4, H=64, T=4, n_dcp=8, dtype="e4m3", slots_per_rank=8192,
+                          seed=seed, device=device, name="long-4x1048576-h64-q4-fp8-dcp8")
+
+
+E2E_LAYERS = 8
+E2E_NCP = 4
+
+
+def e2e_lengths(seed: int = 4) -> list:
+    return log_uniform_lengths(64, 2048, 500_000, seed)

@@ -1,0 +1,335 @@
+/*
+ * dcp_oracle.c -- plain float64 CPU oracle for the decode-context-parallel (DCP) hot path.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only tests/, __graft_entry__.smoke() and the
+ * bench's cpu_baseline / reference leg load this library.  The CUDA library never links,
+ * calls or reads it, and the two share no code, headers, tables or helpers.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [P1] "Serving Macaron-V1 at Scale: Page-Level 2D KV Resharding" (Mind Lab).
+ *   [P2] "SGLang's path" (serving-k3, module 05), paragraph on decode context parallelism.
+ *
+ * Every function restates the pages' definition directly, in float64 where floating point
+ * is involved, with no blocking, fusion or reordering beyond the definition.  Where the pages
+ * leave a step open the reading taken is stated next to the code.
+ *
+ * Parity pins: every function here is pinned by tests/test_oracle_pins.py against worked
+ * examples printed on the pages, closed forms, invariants, library special cases and brute
+ * force on tiny inputs.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define DCPO_PAGE_TOKENS 64  /* [P1] 5.1: pages of 64 tokens                           */
+#define DCPO_K_DIM 576       /* [P1] 5.3: kv_lora_rank + qk_rope_head_dim = 512 + 64    */
+#define DCPO_V_DIM 512       /* absorbed MLA: V is the 512-dim latent part of the row     */
+
+enum { DCPO_BF16 = 0, DCPO_E4M3 = 1 };
+
+int dcpo_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* [P1] 4.1 "Layer Assignment", layer-range equation: contiguous partition of L layers    */
+/* over N_cp ranks with base = floor(L / N_cp) and extra = L mod N_cp; rank r owns         */
+/* [r*base + min(r, extra), (r+1)*base + min(r+1, extra)).                                 */
+/* ------------------------------------------------------------------------------------ */
+void dcpo_layer_range(int n_layers, int n_cp, int r, int *start, int *end) {
+    int base = n_layers / n_cp;
+    int extra = n_layers % n_cp;
+    *start = r * base + (r < extra ? r : extra);
+    *end = (r + 1) * base + (r + 1 < extra ? r + 1 : extra);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* [P1] 5.1 "Page-Level Round-Robin Sharding": owner(p) = p mod N_dcp and                */
+/* slot_local(p) = floor(p / N_dcp).  With N_dcp <= 1 there is a single rank holding the  */
+/* page at slot p ([P1] 6.2: the filter returns the indices unchanged).                   */
+/* ------------------------------------------------------------------------------------ */
+static int page_owner(int32_t v, int n_dcp) { return n_dcp <= 1 ? 0 : (int)(v % n_dcp); }
+static int64_t page_slot(int32_t v, int n_dcp) { return n_dcp <= 1 ? (int64_t)v : (int64_t)(v / n_dcp); }
+
+/* ------------------------------------------------------------------------------------ */
+/* [P1] 6.2 "Page Index Filter": mask(p, d) = [p mod N_dcp == d], filtered = floor(p /    */
+/* N_dcp), kept in input order; identity when N_dcp <= 1.  Returns the kept count.        */
+/* ------------------------------------------------------------------------------------ */
+int64_t dcpo_filter_indices(const int32_t *kv_indices, int64_t n, int n_dcp, int d,
+                            int32_t *out) {
+    int64_t k = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (n_dcp <= 1) {
+            out[k++] = kv_indices[i];
+        } else if (kv_indices[i] % n_dcp == d) {
+            out[k++] = kv_indices[i] / n_dcp;
+        }
+    }
+    return k;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* [P1] 6.3 "Transfer via Mooncake": the ownership mask comes from the decode-side page   */
+/* value (dst mod N_dcp == d); the same mask selects the prefill-side transfer indices,   */
+/* which pass through unchanged, and the kept decode values are divided by N_dcp.         */
+/* ------------------------------------------------------------------------------------ */
+int64_t dcpo_transfer_filter(const int32_t *transfer_idx, const int32_t *dst_idx, int64_t n,
+                             int n_dcp, int d, int32_t *out_src, int32_t *out_dst) {
+    int64_t k = 0;
+    for (int64_t i = 0; i < n; ++i) {
+        if (n_dcp <= 1) {
+            out_src[k] = transfer_idx[i];
+            out_dst[k] = dst_idx[i];
+            ++k;
+        } else if (dst_idx[i] % n_dcp == d) {
+            out_src[k] = transfer_idx[i];
+            out_dst[k] = dst_idx[i] / n_dcp;
+            ++k;
+        }
+    }
+    return k;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* [P1] 2 "Problem Statement" (2D reshard target: for every path (r, d) transfer L_r x   */
+/* P_d) with 6.3 (per layer, filter then write prefill_kv[layer][transfer] into           */
+/* decode_kv[layer][dst]) and 6.4 (the copy unit is the physical 64-token page).          */
+/*                                                                                        */
+/* Layouts (bytes): src_pools[r] : [n_layers(r)][src_pool_pages][page_bytes],            */
+/*                  dst_pools[d] : [n_layers][dst_slots][page_bytes].                     */
+/* Page table: request b owns entries [req_page_ptr[b], req_page_ptr[b+1]) of src_pages   */
+/* (prefill-side page index) and dst_vpages (decode-side global page value).              */
+/* only_src / only_dst restrict to one path coordinate (-1 = all).                        */
+/* Returns 0, or -2 when an index falls outside its pool (nothing is written for it).     */
+/* ------------------------------------------------------------------------------------ */
+int dcpo_reshard(int num_requests, const int64_t *req_page_ptr, const int32_t *src_pages,
+                 const int32_t *dst_vpages, int64_t page_bytes, int n_layers, int n_cp,
+                 uint8_t *const *src_pools, int64_t src_pool_pages, int n_dcp,
+                 uint8_t *const *dst_pools, int64_t dst_slots, int only_src, int only_dst) {
+    int status = 0;
+    int n_dst = n_dcp <= 1 ? 1 : n_dcp;
+    int64_t n_total = req_page_ptr[num_requests];
+    int32_t *kept_src = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n_total > 0 ? n_total : 1));
+    int32_t *kept_dst = (int32_t *)malloc(sizeof(int32_t) * (size_t)(n_total > 0 ? n_total : 1));
+    for (int r = 0; r < n_cp; ++r) {
+        if (only_src >= 0 && r != only_src) continue;
+        int l0, l1;
+        dcpo_layer_range(n_layers, n_cp, r, &l0, &l1);
+        for (int d = 0; d < n_dst; ++d) {
+            if (only_dst >= 0 && d != only_dst) continue;
+            for (int l = l0; l < l1; ++l) {
+                for (int b = 0; b < num_requests; ++b) {
+                    int64_t p0 = req_page_ptr[b], np = req_page_ptr[b + 1] - p0;
+                    int64_t k = dcpo_transfer_filter(src_pages + p0, dst_vpages + p0, np, n_dcp,
+                                                     d, kept_src, kept_dst);
+                    for (int64_t i = 0; i < k; ++i) {
+                        if (kept_src[i] < 0 || kept_src[i] >= src_pool_pages || kept_dst[i] < 0 ||
+                            kept_dst[i] >= dst_slots) {
+                            status = -2;
+                            continue;
+                        }
+                        const uint8_t *src = src_pools[r] +
+                            ((int64_t)(l - l0) * src_pool_pages + kept_src[i]) * page_bytes;
+                        uint8_t *dst = dst_pools[d] + ((int64_t)l * dst_slots + kept_dst[i]) * page_bytes;
+                        memcpy(dst, src, (size_t)page_bytes);
+                    }
+                }
+            }
+        }
+    }
+    free(kept_src);
+    free(kept_dst);
+    return status;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Element decoders, written from the format definitions.                                */
+/* BF16: the upper 16 bits of an IEEE-754 binary32 value.                                */
+/* E4M3 (OCP FP8, "fn" variant): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa      */
+/* bits; exponent 0 is subnormal (m/8 * 2^-6); S.1111.111 is NaN; no infinities.          */
+/* ------------------------------------------------------------------------------------ */
+double dcpo_bf16_value(uint16_t bits) {
+    uint32_t u = (uint32_t)bits << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+double dcpo_e4m3_value(uint8_t bits) {
+    int s = (bits >> 7) & 1;
+    int e = (bits >> 3) & 15;
+    int m = bits & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) {
+        mag = ldexp((double)m / 8.0, -6);
+    } else {
+        mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    }
+    return s ? -mag : mag;
+}
+
+void dcpo_decode_bf16(const uint16_t *in, double *out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = dcpo_bf16_value(in[i]);
+}
+
+void dcpo_decode_e4m3(const uint8_t *in, double *out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = dcpo_e4m3_value(in[i]);
+}
+
+/* One element of a KV row as a real number (kv_scale applied).                          */
+static double kv_element(const void *pool, int dtype, int64_t elem_index, double kv_scale) {
+    if (dtype == DCPO_BF16) return dcpo_bf16_value(((const uint16_t *)pool)[elem_index]);
+    return kv_scale * dcpo_e4m3_value(((const uint8_t *)pool)[elem_index]);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Paged absorbed-MLA decode attention, unsharded or restricted to one DCP rank.          */
+/*                                                                                        */
+/* [P1] 5.2 "DCP Attention": each rank attends over the pages it owns and returns its     */
+/* partial output and LSE; [P2] describes the partial result as an unnormalised weighted  */
+/* sum plus a running log-sum-exp, recombined exactly.  Reading taken: O_d is normalised  */
+/* within rank d's keys (softmax over its own keys) and LSE_d is the natural-log          */
+/* log-sum-exp of rank d's scaled scores; an empty key set gives O = 0, LSE = -inf.        */
+/*                                                                                        */
+/* For request b (n_b tokens, the last T of them new), query token t, head h:             */
+/*   keys   = tokens at positions pos = 64*j + i of logical page j (page-table order)      */
+/*            with pos <= n_b - T + t (causal among the T new tokens; T = 1: all n_b);     */
+/*   s_k    = softmax_scale * sum_{c<576} q[c] * k[c];                                     */
+/*   LSE    = m + ln(sum_k exp(s_k - m)),  m = max_k s_k;                                  */
+/*   O[c]   = sum_k exp(s_k - LSE) * k[c]  for c < 512 (V = the first 512 dims of K).      */
+/* K/V elements are decoded BF16, or E4M3 times kv_scale (one scale for the pool).        */
+/*                                                                                        */
+/* Page j of request b has decode-side page value v = dst_vpages[req_page_ptr[b] + j];     */
+/* it lives in kv_pools[owner(v)] at slot slot(v) (layout [slots][64][576]).              */
+/* rank >= 0 keeps only pages with owner(v) == rank; rank < 0 keeps all pages.            */
+/* rows (length n_rows) lists flat row indices (b*T + t)*H + h to evaluate; NULL = all.   */
+/* Outputs are indexed by the flat row index (o: [rows][512], lse: [rows]).               */
+/* Returns 0, or -2 if a page slot is outside the pool.                                   */
+/* ------------------------------------------------------------------------------------ */
+int dcpo_attention(int num_requests, int q_len, int num_heads, const uint16_t *q,
+                   const int32_t *seq_lens, const int64_t *req_page_ptr,
+                   const int32_t *dst_vpages, int dtype, double kv_scale, double softmax_scale,
+                   int n_dcp, const void *const *kv_pools, int64_t slots_per_rank, int rank,
+                   const int64_t *rows, int64_t n_rows, double *o, double *lse) {
+    int64_t all_rows = (int64_t)num_requests * q_len * num_heads;
+    int64_t count = rows ? n_rows : all_rows;
+    int64_t max_keys = 0;
+    int status = 0;
+    for (int b = 0; b < num_requests; ++b) {
+        int64_t nk = (req_page_ptr[b + 1] - req_page_ptr[b]) * DCPO_PAGE_TOKENS;
+        if (nk > max_keys) max_keys = nk;
+    }
+#pragma omp parallel
+    {
+        double *scores = (double *)malloc(sizeof(double) * (size_t)(max_keys > 0 ? max_keys : 1));
+        const void **key_pool = (const void **)malloc(sizeof(void *) * (size_t)(max_keys > 0 ? max_keys : 1));
+        int64_t *key_row = (int64_t *)malloc(sizeof(int64_t) * (size_t)(max_keys > 0 ? max_keys : 1));
+        double qv[DCPO_K_DIM];
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t ri = 0; ri < count; ++ri) {
+            int64_t row = rows ? rows[ri] : ri;
+            int h = (int)(row % num_heads);
+            int t = (int)((row / num_heads) % q_len);
+            int b = (int)(row / ((int64_t)num_heads * q_len));
+            int64_t limit = (int64_t)seq_lens[b] - q_len + t; /* last visible position */
+            double *o_row = o + (rows ? ri : row) * DCPO_V_DIM;
+            double *lse_row = lse + (rows ? ri : row);
+            for (int c = 0; c < DCPO_K_DIM; ++c)
+                qv[c] = dcpo_bf16_value(q[row * DCPO_K_DIM + c]);
+
+            /* gather this row's keys */
+            int64_t nk = 0;
+            for (int64_t j = 0; j < req_page_ptr[b + 1] - req_page_ptr[b]; ++j) {
+                int32_t v = dst_vpages[req_page_ptr[b] + j];
+                int owner = page_owner(v, n_dcp);
+                int64_t slot = page_slot(v, n_dcp);
+                if (rank >= 0 && owner != rank) continue;
+                if (slot < 0 || slot >= slots_per_rank) {
+#pragma omp atomic write
+                    status = -2;
+                    continue;
+                }
+                for (int i = 0; i < DCPO_PAGE_TOKENS; ++i) {
+                    int64_t pos = j * DCPO_PAGE_TOKENS + i;
+                    if (pos > limit) continue;
+                    key_pool[nk] = kv_pools[owner];
+                    key_row[nk] = slot * DCPO_PAGE_TOKENS + i;
+                    ++nk;
+                }
+            }
+            if (nk == 0) {
+                for (int c = 0; c < DCPO_V_DIM; ++c) o_row[c] = 0.0;
+                *lse_row = -INFINITY;
+                continue;
+            }
+            /* scores */
+            double m = -INFINITY;
+            for (int64_t k = 0; k < nk; ++k) {
+                double dot = 0.0;
+                for (int c = 0; c < DCPO_K_DIM; ++c)
+                    dot += qv[c] * kv_element(key_pool[k], dtype, key_row[k] * DCPO_K_DIM + c, kv_scale);
+                scores[k] = softmax_scale * dot;
+                if (scores[k] > m) m = scores[k];
+            }
+            /* log-sum-exp */
+            double sum = 0.0;
+            for (int64_t k = 0; k < nk; ++k) sum += exp(scores[k] - m);
+            double l = m + log(sum);
+            *lse_row = l;
+            /* normalised weighted sum of V */
+            for (int c = 0; c < DCPO_V_DIM; ++c) o_row[c] = 0.0;
+            for (int64_t k = 0; k < nk; ++k) {
+                double w = exp(scores[k] - l);
+                for (int c = 0; c < DCPO_V_DIM; ++c)
+                    o_row[c] += w * kv_element(key_pool[k], dtype, key_row[k] * DCPO_K_DIM + c, kv_scale);
+            }
+        }
+        free(scores);
+        free(key_pool);
+        free(key_row);
+    }
+    return status;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* [P1] 5.2 "DCP Attention: All-Gather + LSE Merge": LSE_merged = log sum_d exp(LSE_d).   */
+/* [P2]: the partials recombine exactly because softmax normalisation can be deferred.   */
+/* [P1] 8 "EAGLE + DCP Adaptation": ranks are combined in a fixed rank order.             */
+/* Written out: M = max_d LSE_d; w_d = exp(LSE_d - M); LSE = M + ln sum_d w_d;            */
+/* O = sum_d w_d * O_d / sum_d w_d, summed in ascending d.  Parts with LSE = -inf weigh   */
+/* zero; if every part is -inf the row is empty: O = 0, LSE = -inf.                       */
+/* Layouts: o_part [n_parts][rows][v_dim], lse_part [n_parts][rows].                      */
+/* ------------------------------------------------------------------------------------ */
+void dcpo_lse_merge(int n_parts, int64_t rows, int v_dim, const double *o_part,
+                    const double *lse_part, double *o_out, double *lse_out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        double mx = -INFINITY;
+        for (int d = 0; d < n_parts; ++d)
+            if (lse_part[(int64_t)d * rows + r] > mx) mx = lse_part[(int64_t)d * rows + r];
+        double *orow = o_out + r * v_dim;
+        for (int c = 0; c < v_dim; ++c) orow[c] = 0.0;
+        if (mx == -INFINITY) {
+            lse_out[r] = -INFINITY;
+            continue;
+        }
+        double wsum = 0.0;
+        for (int d = 0; d < n_parts; ++d) {
+            double w = exp(lse_part[(int64_t)d * rows + r] - mx);
+            wsum += w;
+            const double *od = o_part + ((int64_t)d * rows + r) * v_dim;
+            for (int c = 0; c < v_dim; ++c) orow[c] += w * od[c];
+        }
+        for (int c = 0; c < v_dim; ++c) orow[c] /= wsum;
+        lse_out[r] = mx + log(wsum);
+    }
+}
