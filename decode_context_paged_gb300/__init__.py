@@ -1,0 +1,235 @@
+"""GB300-native decode context parallelism (DCP) hot path: Python binding of libdcp.so.
+
+The three stages of the method run in hand-written sm_103a CUDA kernels behind the C ABI in
+``include/dcp.h``; this module only marshals torch tensors (device pointers, sizes, the
+current stream) into those calls and turns status codes into exceptions.  There is no CPU
+fallback: if ``libdcp.so`` is missing or the GPU is absent the calls raise.
+
+Entry points (same names as the C ABI):
+  layer_range              CP layer split ("Serving Macaron-V1 at Scale", 4.1)
+  filter_page_indices      source-side page-index filter (6.2, 6.3)
+  reshard_pages            CP layer-split -> DCP page reshard, all paths in one launch (2, 6.3, 6.4)
+  partial_decode_attn      per-rank paged MLA decode attention -> partial O + LSE (5.2)
+  lse_merge                exact LSE merge of the partials (5.2)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdcp.so")
+
+DCP_OK = 0
+DCP_KV_BF16 = 0
+DCP_KV_FP8_E4M3 = 1
+DEVERR_OUT_OF_RANGE = 0x1
+DEVERR_TIMEOUT = 0x2
+PAGE = 64
+K_DIM = 576
+V_DIM = 512
+
+_lib = None
+
+
+class DcpError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                              "(nvcc, sm_103a); there is no fallback path")
+        lib = ctypes.CDLL(LIB_PATH)
+        i32, i64, f32, vp, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+        lib.dcp_version.restype = i32
+        lib.dcp_status_string.argtypes = [i32]
+        lib.dcp_status_string.restype = ctypes.c_char_p
+        lib.dcp_device_error_status.argtypes = [ctypes.c_int32]
+        lib.dcp_device_error_status.restype = i32
+        lib.dcp_layer_range.argtypes = [i32, i32, i32, vp, vp]
+        lib.dcp_layer_range.restype = i32
+        lib.dcp_filter_page_indices.argtypes = [i64, vp, vp, i32, i32, vp, vp, vp, vp]
+        lib.dcp_filter_page_indices.restype = i32
+        lib.dcp_reshard_pages.argtypes = [i32, vp, i64, vp, vp, i32, i32, i32, i32, i32, vp, i64, i32,
+                                          vp, i64, i32, i32, vp, vp]
+        lib.dcp_reshard_pages.restype = i32
+        lib.dcp_partial_decode_attn_workspace_size.argtypes = [i32, i32, i32, i32, i64]
+        lib.dcp_partial_decode_attn_workspace_size.restype = sz
+        lib.dcp_partial_decode_attn.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, f32, i32,
+                                                vp, i64, i32, vp, vp, vp, sz, vp, vp]
+        lib.dcp_partial_decode_attn.restype = i32
+        lib.dcp_lse_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp, vp]
+        lib.dcp_lse_merge.restype = i32
+        _lib = lib
+    return _lib
+
+
+def library():
+    """The loaded ctypes handle of libdcp.so."""
+    return _load()
+
+
+def version() -> int:
+    return int(_load().dcp_version())
+
+
+def status_string(status: int) -> str:
+    return _load().dcp_status_string(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != DCP_OK:
+        raise DcpError(status, what)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream or None
+
+
+def _dptr(t: torch.Tensor | None, name: str, dtype=None, device=True) -> int | None:
+    if t is None:
+        return None
+    if device and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _kv_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return DCP_KV_BF16
+    if t.dtype == torch.float8_e4m3fn:
+        return DCP_KV_FP8_E4M3
+    raise ValueError(f"KV pools must be bfloat16 or float8_e4m3fn, got {t.dtype}")
+
+
+def _ptr_array(tensors, name) -> ctypes.Array:
+    return (ctypes.c_void_p * len(tensors))(*[_dptr(t, f"{name}[{i}]") for i, t in enumerate(tensors)])
+
+
+def device_error_status(word: int) -> int:
+    return int(_load().dcp_device_error_status(int(word)))
+
+
+def layer_range(n_layers: int, n_cp: int, r: int) -> tuple[int, int]:
+    s, e = ctypes.c_int(0), ctypes.c_int(0)
+    _check(_load().dcp_layer_range(n_layers, n_cp, r, ctypes.addressof(s), ctypes.addressof(e)),
+           "dcp_layer_range")
+    return s.value, e.value
+
+
+def filter_page_indices(dst_vpages: torch.Tensor, n_dcp: int, d: int,
+                        transfer_idx: torch.Tensor | None = None, stream=None):
+    """Returns (slots, src or None, count tensor); the first ``count`` entries are valid."""
+    n = dst_vpages.numel()
+    out_slot = torch.empty(max(n, 1), dtype=torch.int32, device=dst_vpages.device)
+    out_src = torch.empty_like(out_slot) if transfer_idx is not None else None
+    count = torch.zeros(1, dtype=torch.int64, device=dst_vpages.device)
+    _check(_load().dcp_filter_page_indices(n, _dptr(dst_vpages, "dst_vpages", torch.int32),
+                                           _dptr(transfer_idx, "transfer_idx", torch.int32), n_dcp, d,
+                                           _dptr(out_slot, "out_slot"), _dptr(out_src, "out_src"),
+                                           _dptr(count, "count"), _stream(stream)),
+           "dcp_filter_page_indices")
+    return out_slot, out_src, count
+
+
+def reshard_pages(req_page_ptr: torch.Tensor, src_pages: torch.Tensor, dst_vpages: torch.Tensor,
+                  num_layers: int, src_pools: list, src_pool_pages: int, dst_pools: list,
+                  dst_slots_per_rank: int, n_dcp: int | None = None, only_src_rank: int = -1,
+                  only_dst_rank: int = -1, dev_error: torch.Tensor | None = None, stream=None) -> None:
+    """Page-level reshard (all (r, d) paths in one launch); dst_pools are written in place."""
+    dtype = _kv_code(src_pools[0])
+    n_dcp = len(dst_pools) if n_dcp is None else n_dcp
+    sp = _ptr_array(src_pools, "src_pools")
+    dp = _ptr_array(dst_pools, "dst_pools")
+    _check(_load().dcp_reshard_pages(req_page_ptr.numel() - 1, _dptr(req_page_ptr, "req_page_ptr", torch.int64),
+                                     dst_vpages.numel(), _dptr(src_pages, "src_pages", torch.int32),
+                                     _dptr(dst_vpages, "dst_vpages", torch.int32), PAGE, K_DIM, dtype,
+                                     num_layers, len(src_pools), ctypes.addressof(sp), src_pool_pages,
+                                     n_dcp, ctypes.addressof(dp), dst_slots_per_rank, only_src_rank,
+                                     only_dst_rank, _dptr(dev_error, "dev_error", torch.int32),
+                                     _stream(stream)),
+           "dcp_reshard_pages")
+
+
+def workspace_size(num_requests: int, q_len: int, num_heads: int, n_dcp: int, num_pages: int) -> int:
+    return int(_load().dcp_partial_decode_attn_workspace_size(num_requests, q_len, num_heads, n_dcp,
+                                                              num_pages))
+
+
+def alloc_workspace(num_requests: int, q_len: int, num_heads: int, n_dcp: int, num_pages: int,
+                    device) -> torch.Tensor:
+    n = workspace_size(num_requests, q_len, num_heads, n_dcp, num_pages)
+    if n == 0:
+        raise DcpError(-1, "dcp_partial_decode_attn_workspace_size")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def partial_decode_attn(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: torch.Tensor,
+                        dst_vpages: torch.Tensor, kv_pools: list, softmax_scale: float,
+                        kv_scale: float = 1.0, only_rank: int = -1, o_part: torch.Tensor | None = None,
+                        lse_part: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                        dev_error: torch.Tensor | None = None, stream=None):
+    """Per-rank partial attention.  q: bf16 [B][T][H][576]; kv_pools: per-rank [slots][64][576].
+    Returns (o_part [N][B][T][H][512] fp32, lse_part [N][B][T][H] fp32)."""
+    B, T, H, kd = q.shape
+    if kd != K_DIM:
+        raise ValueError("q must be [B][T][H][576]")
+    N = len(kv_pools)
+    slots = kv_pools[0].shape[0]
+    dtype = _kv_code(kv_pools[0])
+    for p in kv_pools:
+        if p.shape != (slots, PAGE, K_DIM) or p.dtype != kv_pools[0].dtype:
+            raise ValueError("every kv pool must be [slots][64][576] of one dtype")
+    dev = q.device
+    if o_part is None:
+        o_part = torch.empty((N, B, T, H, V_DIM), dtype=torch.float32, device=dev)
+    if lse_part is None:
+        lse_part = torch.empty((N, B, T, H), dtype=torch.float32, device=dev)
+    num_pages = dst_vpages.numel()
+    if workspace is None:
+        workspace = alloc_workspace(B, T, H, N, num_pages, dev)
+    kp = _ptr_array(kv_pools, "kv_pools")
+    _check(_load().dcp_partial_decode_attn(B, T, H, _dptr(q, "q", torch.bfloat16),
+                                           _dptr(seq_lens, "seq_lens", torch.int32),
+                                           _dptr(req_page_ptr, "req_page_ptr", torch.int64), num_pages,
+                                           _dptr(dst_vpages, "dst_vpages", torch.int32), PAGE, dtype,
+                                           float(kv_scale), float(softmax_scale), N, ctypes.addressof(kp),
+                                           slots, only_rank, _dptr(o_part, "o_part", torch.float32),
+                                           _dptr(lse_part, "lse_part", torch.float32),
+                                           _dptr(workspace, "workspace"), workspace.numel(),
+                                           _dptr(dev_error, "dev_error", torch.int32), _stream(stream)),
+           "dcp_partial_decode_attn")
+    return o_part, lse_part
+
+
+def lse_merge(o_part: torch.Tensor, lse_part: torch.Tensor, o_out: torch.Tensor | None = None,
+              lse_out: torch.Tensor | None = None, stream=None):
+    """Merge [N][rows...][v] partials into [rows...][v]; returns (o, lse)."""
+    n = o_part.shape[0]
+    v = o_part.shape[-1]
+    rows = lse_part[0].numel()
+    if o_part.numel() != n * rows * v:
+        raise ValueError("o_part / lse_part shapes disagree")
+    if o_out is None:
+        o_out = torch.empty(o_part.shape[1:], dtype=torch.float32, device=o_part.device)
+    if lse_out is None:
+        lse_out = torch.empty(lse_part.shape[1:], dtype=torch.float32, device=o_part.device)
+    _check(_load().dcp_lse_merge(n, rows, v, _dptr(o_part, "o_part", torch.float32),
+                                 _dptr(lse_part, "lse_part", torch.float32),
+                                 _dptr(o_out, "o_out", torch.float32), _dptr(lse_out, "lse_out", torch.float32),
+                                 _stream(stream)),
+           "dcp_lse_merge")
+    return o_out, lse_out

@@ -1,0 +1,90 @@
+// dcp_internal.h -- declarations shared between the library's translation units (host side).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/dcp.h"
+
+namespace dcp {
+
+constexpr int kPage = DCP_PAGE_TOKENS;
+constexpr int kKDim = DCP_K_DIM;
+constexpr int kVDim = DCP_V_DIM;
+constexpr int kMaxCp = 64;
+constexpr int kMaxDcpReshard = 64;
+constexpr int kMaxDcpAttn = DCP_MAX_RANKS;
+
+// Default limit for one device-side pipeline wait (nanoseconds of wall time).
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+// ---- reshard (dcp_reshard.cu)
+struct ReshardArgs {
+    const int64_t *req_page_ptr;
+    const int32_t *src_pages;
+    const int32_t *dst_vpages;
+    int num_requests;
+    int64_t num_pages;
+    int64_t page_bytes;
+    int layer_begin;                 // layers [layer_begin, layer_end) are moved
+    int layer_end;
+    int n_cp;
+    int layer_start[kMaxCp + 1];     // source rank r owns [layer_start[r], layer_start[r+1])
+    const uint8_t *src_pools[kMaxCp];
+    int64_t src_pool_pages;
+    int n_dcp;
+    uint8_t *dst_pools[kMaxDcpReshard];
+    int64_t dst_slots;
+    int only_dst;
+    int32_t *dev_error;
+    uint64_t wait_limit_ns;
+};
+cudaError_t launch_reshard(const ReshardArgs &a, int num_sms, cudaStream_t stream);
+
+cudaError_t launch_filter(int64_t n, const int32_t *dst_vpages, const int32_t *transfer_idx,
+                          int n_dcp, int d, int32_t *out_slot, int32_t *out_src,
+                          int64_t *out_count, cudaStream_t stream);
+
+// ---- merge (dcp_merge.cu)
+cudaError_t launch_lse_merge(int n_parts, int64_t rows, int v_dim, const float *o_part,
+                             const float *lse_part, float *o_out, float *lse_out,
+                             cudaStream_t stream);
+
+// ---- attention (dcp_attn.cu)
+struct AttnPlanShape {
+    int B, T, H, N, G, heads_per_group;
+    int64_t num_pages;
+    int tiles_per_chunk;
+    int64_t max_units;
+    int64_t max_partials;
+    int64_t n_seg;
+    size_t off_counts, off_slots, off_pages, off_units, off_seg, off_ctrl, off_part_o,
+        off_part_lse;
+    size_t total_bytes;
+};
+bool plan_attention(int B, int T, int H, int N, int64_t num_pages, int dtype, int num_sms,
+                    AttnPlanShape *out);
+
+struct AttnArgs {
+    AttnPlanShape shape;
+    const void *q;
+    const int32_t *seq_lens;
+    const int64_t *req_page_ptr;
+    const int32_t *dst_vpages;
+    int dtype;
+    float kv_scale;
+    float softmax_scale;
+    const void *kv_pools[kMaxDcpAttn];
+    int64_t slots_per_rank;
+    int only_rank;
+    float *o_part;
+    float *lse_part;
+    uint8_t *workspace;
+    int32_t *dev_error;
+    uint64_t wait_limit_ns;
+};
+int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream);
+
+}  // namespace dcp

@@ -1,0 +1,187 @@
+// dcp_reshard.cu -- page-level 2D KV reshard (CP layer-split -> DCP page-interleaved) and the
+// source-side page-index filter.
+//
+// "Serving Macaron-V1 at Scale: Page-Level 2D KV Resharding":
+//   2 (2D reshard target: every path (r, d) moves L_r x P_d), 5.1 (owner = p mod N_dcp,
+//   local slot = p div N_dcp), 6.2 (page index filter), 6.3 (mask on the decode-side page
+//   value, source indices pass through), 6.4 (the copy unit is the physical 64-token page).
+//
+// The reshard is a pure HBM->HBM byte move: every (layer, page) item is one contiguous page
+// read and one contiguous page written.  One CTA per SM runs a single issuing thread that
+// streams 18 KB chunks through an 11-stage shared-memory ring with TMA bulk copies
+// (cp.async.bulk global->shared completing on an mbarrier, then shared->global in bulk
+// groups), keeping ~8 loads and ~3 stores in flight per SM.  Work is split as contiguous
+// chunk ranges of the flattened (layer, page, chunk) space; all (r, d) paths share the launch.
+#include <cuda_runtime.h>
+
+#include "dcp_internal.h"
+#include "dcp_ptx.cuh"
+
+namespace dcp {
+namespace {
+
+constexpr uint32_t kChunk = 18432;  // divides both page sizes (73,728 and 36,864 bytes)
+constexpr int kStages = 11;
+constexpr int kLag = 8;             // loads kept ahead of stores
+static_assert(kStages - kLag - 1 >= 0, "ring too small for the lag");
+constexpr size_t kReshardSmem = (size_t)kStages * kChunk + kStages * sizeof(uint64_t);
+
+__global__ void __launch_bounds__(32, 1) reshard_kernel(const __grid_constant__ ReshardArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * kChunk);
+    __shared__ int abort_flag;
+    if (threadIdx.x != 0) return;
+    abort_flag = 0;
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+    fence_proxy_async_smem();
+
+    const int64_t cpp = a.page_bytes / kChunk;  // chunks per page
+    const int64_t n_layers = a.layer_end - a.layer_begin;
+    const int64_t total = n_layers * a.num_pages * cpp;
+    const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+    const int64_t c_begin = (int64_t)blockIdx.x * per;
+    const int64_t c_end = c_begin + per < total ? c_begin + per : total;
+
+    uint8_t *store_dst[kStages] = {};
+    int64_t issued = 0, stored = 0;
+    bool ok = true;
+    int r = 0;
+
+    auto store_one = [&]() -> bool {
+        const int stage = (int)(stored % kStages);
+        const uint32_t parity = (uint32_t)((stored / kStages) & 1);
+        if (!mbar_wait(&bars[stage], parity, &abort_flag, a.dev_error, a.wait_limit_ns)) return false;
+        bulk_s2g(store_dst[stage], smem + (size_t)stage * kChunk, kChunk);
+        bulk_commit();
+        ++stored;
+        return true;
+    };
+
+    for (int64_t c = c_begin; c < c_end && ok; ++c) {
+        const int64_t item = c / cpp;
+        const int64_t part = c - item * cpp;
+        const int l = a.layer_begin + (int)(item / a.num_pages);
+        const int64_t p = item - (int64_t)(l - a.layer_begin) * a.num_pages;
+        while (r + 1 < a.n_cp && l >= a.layer_start[r + 1]) ++r;
+        while (r > 0 && l < a.layer_start[r]) --r;
+        const int32_t v = __ldg(a.dst_vpages + p);
+        const int32_t src_idx = __ldg(a.src_pages + p);
+        int d;
+        int64_t slot;
+        if (a.n_dcp <= 1) {
+            d = 0;
+            slot = v;
+        } else {
+            d = v % a.n_dcp;
+            slot = v / a.n_dcp;
+        }
+        if (v < 0 || slot >= a.dst_slots || src_idx < 0 || src_idx >= a.src_pool_pages) {
+            if (part == 0 && a.dev_error) atomicOr(a.dev_error, DCP_DEVERR_OUT_OF_RANGE);
+            continue;
+        }
+        if (a.only_dst >= 0 && d != a.only_dst) continue;
+        const uint8_t *src = a.src_pools[r] +
+                             ((int64_t)(l - a.layer_start[r]) * a.src_pool_pages + src_idx) * a.page_bytes +
+                             part * kChunk;
+        uint8_t *dst = a.dst_pools[d] + ((int64_t)l * a.dst_slots + slot) * a.page_bytes + part * kChunk;
+
+        const int stage = (int)(issued % kStages);
+        if (issued >= kStages) bulk_wait_read<kStages - kLag - 1>();  // stage's old store has read smem
+        mbar_arrive_expect_tx(&bars[stage], kChunk);
+        bulk_g2s(smem + (size_t)stage * kChunk, src, kChunk, &bars[stage]);
+        store_dst[stage] = dst;
+        ++issued;
+        while (issued - stored > kLag && ok) ok = store_one();
+    }
+    while (ok && stored < issued) ok = store_one();
+    bulk_wait<0>();
+    if (!ok) {
+        // A load wait gave up: let the copies already issued land before the CTA exits.
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < 200000ull) {
+        }
+    }
+}
+
+// Stable single-block compaction: keep entries whose decode-side page value belongs to rank d.
+constexpr int kFilterThreads = 1024;
+constexpr int kFilterItems = 8;
+
+__global__ void __launch_bounds__(kFilterThreads)
+filter_kernel(int64_t n, const int32_t *__restrict__ dst_vpages,
+              const int32_t *__restrict__ transfer_idx, int n_dcp, int d,
+              int32_t *__restrict__ out_slot, int32_t *__restrict__ out_src,
+              int64_t *__restrict__ out_count) {
+    __shared__ int warp_tot[kFilterThreads / 32];
+    __shared__ int64_t running;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) running = 0;
+    __syncthreads();
+    for (int64_t base = 0; base < n; base += (int64_t)kFilterThreads * kFilterItems) {
+        const int64_t i0 = base + (int64_t)tid * kFilterItems;
+        int keep = 0;
+        int32_t vals[kFilterItems];
+#pragma unroll
+        for (int k = 0; k < kFilterItems; ++k) {
+            const int64_t i = i0 + k;
+            vals[k] = i < n ? __ldg(dst_vpages + i) : -1;
+            const bool kept = i < n && (n_dcp <= 1 || vals[k] % n_dcp == d);
+            keep |= (int)kept << k;
+        }
+        const int cnt = __popc(keep);
+        int incl = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int t = warp_tot[lane];
+            int s = t;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, s, o);
+                if (lane >= o) s += y;
+            }
+            warp_tot[lane] = s - t;  // exclusive prefix over warps
+        }
+        __syncthreads();
+        int64_t pos = running + warp_tot[warp] + (incl - cnt);
+#pragma unroll
+        for (int k = 0; k < kFilterItems; ++k) {
+            if (keep & (1 << k)) {
+                out_slot[pos] = n_dcp <= 1 ? vals[k] : vals[k] / n_dcp;
+                if (transfer_idx) out_src[pos] = __ldg(transfer_idx + i0 + k);
+                ++pos;
+            }
+        }
+        __syncthreads();
+        if (tid == kFilterThreads - 1) running = pos;
+        __syncthreads();
+    }
+    if (tid == 0) *out_count = running;
+}
+
+}  // namespace
+
+cudaError_t launch_reshard(const ReshardArgs &a, int num_sms, cudaStream_t stream) {
+    if ((a.layer_end - a.layer_begin) <= 0 || a.num_pages <= 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(reshard_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kReshardSmem);
+    if (e != cudaSuccess) return e;
+    reshard_kernel<<<num_sms, 32, kReshardSmem, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_filter(int64_t n, const int32_t *dst_vpages, const int32_t *transfer_idx,
+                          int n_dcp, int d, int32_t *out_slot, int32_t *out_src,
+                          int64_t *out_count, cudaStream_t stream) {
+    filter_kernel<<<1, kFilterThreads, 0, stream>>>(n, dst_vpages, transfer_idx, n_dcp, d, out_slot,
+                                                     out_src, out_count);
+    return cudaGetLastError();
+}
+
+}  // namespace dcp

@@ -1,0 +1,192 @@
+/*
+ * dcp.h -- C ABI of libdcp.so, the GB300 (sm_103a) hot path of decode context parallelism.
+ *
+ * The method (cited by page title and section):
+ *   [P1] "Serving Macaron-V1 at Scale: Page-Level 2D KV Resharding" (Mind Lab).
+ *   [P2] "SGLang's path" (serving-k3, module 05), paragraph on decode context parallelism.
+ *
+ * A decode group of N_dcp ranks shards a request's KV cache by page: page value p belongs to
+ * rank p mod N_dcp at local slot p div N_dcp ([P1] 5.1).  The prefill side holds whole layers
+ * per CP rank ([P1] 4.1).  Three stages run on one GPU, the N_dcp ranks being N_dcp pools in
+ * its memory:
+ *   dcp_reshard_pages        -- page gather/scatter CP layer-split -> DCP pages ([P1] 2, 6.2-6.4)
+ *   dcp_partial_decode_attn  -- paged absorbed-MLA decode attention per rank ([P1] 5.2, [P2])
+ *   dcp_lse_merge            -- exact log-sum-exp recombination of the partials ([P1] 5.2, [P2])
+ * plus dcp_filter_page_indices (the source-side index filter of [P1] 6.2/6.3 on its own) and
+ * dcp_layer_range (the layer split of [P1] 4.1, a host function).
+ *
+ * Conventions shared by every entry point:
+ *   - KV rows are 576 elements (512 latent + 64 rope, [P1] 5.3); V is the first 512 of them.
+ *     A page is 64 rows stored contiguously: [64][576].  BF16 page = 73,728 bytes; FP8-E4M3
+ *     page = 36,864 bytes.  Pool bases must be 16-byte aligned.
+ *   - A "page value" v is the decode-side global page number: v = slot * N_dcp + owner.
+ *   - Pointers are device pointers unless the comment says host.  The caller owns every
+ *     buffer; the library allocates nothing and keeps no state between calls.  Outputs must
+ *     not alias inputs.
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).  Argument and
+ *     shape errors are detected on the host before anything is launched and return a
+ *     negative dcp_status.  Problems only visible on the device (a page value or index
+ *     outside its pool, a pipeline wait that ran past its time limit) are OR-ed into the
+ *     optional device word `dev_error` (DCP_DEVERR_* bits; pass NULL to ignore) and the
+ *     offending page is skipped; nothing traps.  Read the word after synchronising.
+ *   - Thread-safe: no global mutable state.
+ */
+#ifndef DCP_H_
+#define DCP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *dcp_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    DCP_OK = 0,
+    DCP_ERR_INVALID_ARG = -1,  /* null pointer, bad size, unsupported combination      */
+    DCP_ERR_OUT_OF_RANGE = -2, /* an index outside its pool (reported via dev_error)    */
+    DCP_ERR_UNSUPPORTED = -3,  /* valid request this build does not implement           */
+    DCP_ERR_WORKSPACE = -4,    /* workspace missing, too small or misaligned            */
+    DCP_ERR_CUDA = -5,         /* a CUDA runtime call failed (launch, attribute, ...)   */
+    DCP_ERR_TIMEOUT = -6       /* a device pipeline wait ran past its limit             */
+} dcp_status;
+
+typedef enum { DCP_KV_BF16 = 0, DCP_KV_FP8_E4M3 = 1 } dcp_kv_dtype;
+
+/* Bits OR-ed into *dev_error by kernels. */
+#define DCP_DEVERR_OUT_OF_RANGE 0x1 /* page value / source index outside its pool       */
+#define DCP_DEVERR_TIMEOUT 0x2      /* an mbarrier wait exceeded its limit; unit skipped */
+
+#define DCP_PAGE_TOKENS 64
+#define DCP_K_DIM 576
+#define DCP_V_DIM 512
+#define DCP_MAX_RANKS 16
+
+/* Library version, major*10000 + minor*100 + patch. */
+int dcp_version(void);
+
+/* Static description of a status code. */
+const char *dcp_status_string(int status);
+
+/* Maps a device error word to a status: 0 -> DCP_OK, TIMEOUT bit -> DCP_ERR_TIMEOUT,
+ * OUT_OF_RANGE bit -> DCP_ERR_OUT_OF_RANGE. */
+int dcp_device_error_status(int32_t dev_error_word);
+
+/*
+ * [P1] 4.1 "Layer Assignment", layer-range equation.  Host function.
+ * Rank r of n_cp owns layers [start, end) with base = n_layers div n_cp,
+ * extra = n_layers mod n_cp, start = r*base + min(r, extra), end = start + base + (r < extra).
+ * Returns DCP_ERR_INVALID_ARG if n_layers < 0, n_cp < 1, r outside [0, n_cp) or a null output.
+ */
+int dcp_layer_range(int n_layers, int n_cp, int r, int *start, int *end);
+
+/*
+ * [P1] 6.2 "Page Index Filter" and 6.3 "Transfer via Mooncake": the source-side filter for
+ * decode rank d.  For i in [0, n) in order, entry i is kept iff n_dcp <= 1 or
+ * dst_vpages[i] mod n_dcp == d; kept entries write out_slot[k] = dst_vpages[i] div n_dcp
+ * (dst_vpages[i] itself when n_dcp <= 1) and, if transfer_idx is non-NULL,
+ * out_src[k] = transfer_idx[i] unchanged.  The kept count is written to *out_count
+ * (device int64).  Output order is the input order (stable).
+ *   dst_vpages   int32 [n]  decode-side page values (non-negative)
+ *   transfer_idx int32 [n]  prefill-side page indices, or NULL
+ *   out_slot     int32 [n]  capacity n;  out_src int32 [n] or NULL (required if transfer_idx)
+ * Returns DCP_ERR_INVALID_ARG for n < 0, n_dcp < 1, d outside [0, max(n_dcp,1)), null
+ * required pointers; DCP_ERR_CUDA if the launch fails.
+ */
+int dcp_filter_page_indices(int64_t n, const int32_t *dst_vpages, const int32_t *transfer_idx,
+                            int n_dcp, int d, int32_t *out_slot, int32_t *out_src,
+                            int64_t *out_count, dcp_stream_t stream);
+
+/*
+ * [P1] 2 "Problem Statement" (2D reshard target), 6.3 and 6.4: the page-level reshard from a
+ * CP layer-split source layout into the DCP page-interleaved destination layout, every
+ * (source rank r, destination rank d) path in one launch.  For every layer l (owned by
+ * source rank r per dcp_layer_range), every request b and every page entry i of b in
+ * [req_page_ptr[b], req_page_ptr[b+1]) with v = dst_vpages[i], owner d = v mod n_dcp and
+ * slot v div n_dcp (single rank, slot v, when n_dcp == 1):
+ *     dst_pools[d][l][slot]  <-  src_pools[r][l - start_r][src_pages[i]]      (one page)
+ * Bytes are copied exactly.  Destination slots named by no entry are left untouched.
+ *   num_requests >= 0; req_page_ptr int64 [num_requests+1] (device), non-decreasing from 0.
+ *   src_pages int32 [pages], dst_vpages int32 [pages]  (pages = req_page_ptr[num_requests],
+ *     passed again as num_pages so the host need not read device memory).
+ *   page_size must be 64 and row_elems 576.
+ *   src_pools: HOST array [n_cp] of device pointers; src_pools[r] is
+ *     [layers of r][src_pool_pages][64][576] elements.
+ *   dst_pools: HOST array [n_dcp] of device pointers; dst_pools[d] is
+ *     [num_layers][dst_slots_per_rank][64][576].
+ *   only_src_rank / only_dst_rank: restrict to one path coordinate (-1 = all).
+ *   Entries whose source index or slot fall outside their pool set DCP_DEVERR_OUT_OF_RANGE
+ *   and are skipped.  Duplicate page values in the table are the caller's error (the last
+ *   writer wins in an unspecified order).
+ * Returns DCP_ERR_INVALID_ARG for bad shapes, ranks (1 <= n_cp, n_dcp <= 64), null
+ * pointers or unaligned pools; DCP_ERR_CUDA on launch failure.
+ */
+int dcp_reshard_pages(int num_requests, const int64_t *req_page_ptr, int64_t num_pages,
+                      const int32_t *src_pages, const int32_t *dst_vpages, int page_size,
+                      int row_elems, int dtype, int num_layers, int n_cp,
+                      const void *const *src_pools, int64_t src_pool_pages, int n_dcp,
+                      void *const *dst_pools, int64_t dst_slots_per_rank, int only_src_rank,
+                      int only_dst_rank, int32_t *dev_error, dcp_stream_t stream);
+
+/*
+ * Device workspace (bytes) dcp_partial_decode_attn needs for these sizes.  The result
+ * depends only on the arguments and on the current device's SM count.  Returns 0 for
+ * invalid sizes.
+ */
+size_t dcp_partial_decode_attn_workspace_size(int num_requests, int q_len, int num_heads,
+                                              int n_dcp, int64_t num_pages);
+
+/*
+ * [P1] 5.2 "DCP Attention", [P2] (partial result plus log-sum-exp): paged absorbed-MLA
+ * decode attention of every query row over each DCP rank's own pages, one launch for all
+ * ranks (only_rank = -1) or for one rank.
+ * For rank d, request b, new token t in [0, q_len), head h, over the keys of b's pages owned
+ * by d at positions pos = 64*j + i (j = page index within b, i = row) with
+ * pos <= seq_lens[b] - q_len + t  (causal among the q_len new tokens):
+ *     s_k = softmax_scale * kappa * (q . k_raw),  LSE_d = ln sum_k exp(s_k),
+ *     O_d = sum_k exp(s_k - LSE_d) * kappa * v_raw[0:512]
+ * with kappa = kv_scale for FP8-E4M3 pools and 1 for BF16.  A rank with no visible key
+ * writes O_d = 0 and LSE_d = -inf.
+ *   q        bf16 [num_requests][q_len][num_heads][576]
+ *   seq_lens int32 [num_requests], tokens of b including the q_len new ones (>= q_len)
+ *   req_page_ptr int64 [num_requests+1], dst_vpages int32 [num_pages]: page table
+ *   kv_pools HOST array [n_dcp] of device pointers, each one layer: [slots_per_rank][64][576]
+ *            (BF16 or E4M3 per dtype).  Rows at positions >= seq_lens[b] in a request's last
+ *            page are masked but must hold finite values.
+ *   o_part   fp32 [n_dcp][num_requests][q_len][num_heads][512]
+ *   lse_part fp32 [n_dcp][num_requests][q_len][num_heads]  (natural log)
+ *   With only_rank = d >= 0 only rank d's slices of o_part / lse_part are written.
+ *   workspace: device, >= dcp_partial_decode_attn_workspace_size(...) bytes, 256-byte aligned.
+ * Page values outside [0, slots_per_rank * n_dcp) set DCP_DEVERR_OUT_OF_RANGE and the page is
+ * skipped.  Returns DCP_ERR_INVALID_ARG (shapes, null pointers, page_size != 64,
+ * 1 <= n_dcp <= 16, q_len >= 1, num_heads >= 1), DCP_ERR_WORKSPACE, DCP_ERR_CUDA.
+ */
+int dcp_partial_decode_attn(int num_requests, int q_len, int num_heads, const void *q,
+                            const int32_t *seq_lens, const int64_t *req_page_ptr,
+                            int64_t num_pages, const int32_t *dst_vpages, int page_size,
+                            int dtype, float kv_scale, float softmax_scale, int n_dcp,
+                            const void *const *kv_pools, int64_t slots_per_rank, int only_rank,
+                            float *o_part, float *lse_part, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_error, dcp_stream_t stream);
+
+/*
+ * [P1] 5.2 "All-Gather + LSE Merge" (LSE_merged = log sum_d exp LSE_d) and [P2] (exact
+ * recombination): per row r, M = max_d LSE_d, w_d = exp(LSE_d - M),
+ *     LSE[r] = M + ln sum_d w_d,   O[r] = sum_d w_d O_d[r] / sum_d w_d,
+ * summed in ascending d ([P1] 8: fixed rank order).  Parts with LSE = -inf weigh zero;
+ * a row whose parts are all -inf gets O = 0, LSE = -inf.
+ *   o_part fp32 [n_parts][rows][v_dim], lse_part fp32 [n_parts][rows]
+ *   o_out  fp32 [rows][v_dim],           lse_out  fp32 [rows]
+ *   1 <= n_parts <= 64, rows >= 0, v_dim in {128, 256, 512}; 16-byte aligned O arrays.
+ * Returns DCP_ERR_INVALID_ARG or DCP_ERR_CUDA.
+ */
+int dcp_lse_merge(int n_parts, int64_t rows, int v_dim, const float *o_part,
+                  const float *lse_part, float *o_out, float *lse_out, dcp_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DCP_H_ */

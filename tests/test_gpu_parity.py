@@ -1,0 +1,184 @@
+"""GPU parity: the CUDA path (through the C ABI) against the float64 oracle.
+
+Reshard and index filtering must match bit for bit; attention and merge outputs within
+2e-2 max-abs on O and 1e-3 on LSE.  Sizes span several 128-token tiles and ragged tails;
+the full-size workloads are checked on sampled rows the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import dcp_inputs as di
+import decode_context_paged_gb300 as dcp
+import oracle
+from _parity import compare, oracle_attention, pool_bytes, q_bits
+
+pytestmark = pytest.mark.gpu
+
+
+# ----------------------------------------------------------------------------- merge
+@pytest.mark.parametrize("n,rows", [(1, 7), (4, 300), (8, 1024), (3, 1)])
+def test_lse_merge_matches_oracle(cuda_device, n, rows):
+    g = torch.Generator().manual_seed(n * 1000 + rows)
+    o = torch.randn((n, rows, 512), generator=g, dtype=torch.float32)
+    lse = 4 * torch.randn((n, rows), generator=g, dtype=torch.float32)
+    if n > 1:
+        lse[0, ::5] = -float("inf")           # empty shards
+    lse[:, rows // 2] = -float("inf")         # an all-empty row
+    o_gpu, l_gpu = dcp.lse_merge(o.to(cuda_device), lse.to(cuda_device))
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.lse_merge(o.double().numpy(), lse.double().numpy())
+    compare(o_gpu.cpu().numpy(), l_gpu.cpu().numpy(), o_ref, l_ref, "merge", o_tol=1e-5, lse_tol=1e-5)
+
+
+# ---------------------------------------------------------------------------- filter
+@pytest.mark.parametrize("n_dcp,n", [(1, 100), (4, 256), (8, 20000), (3, 1), (8, 0)])
+def test_filter_matches_oracle_bit_exact(cuda_device, n_dcp, n):
+    g = torch.Generator().manual_seed(n + n_dcp)
+    vals = torch.randperm(max(4 * n, 1), generator=g)[:n].to(torch.int32)
+    src = torch.randperm(max(4 * n, 1), generator=g)[:n].to(torch.int32)
+    for d in range(n_dcp):
+        slot, s, cnt = dcp.filter_page_indices(vals.to(cuda_device), n_dcp, d, src.to(cuda_device))
+        torch.cuda.synchronize()
+        k = int(cnt.item())
+        ref_src, ref_dst = oracle.transfer_filter(src.numpy(), vals.numpy(), n_dcp, d)
+        assert k == ref_dst.size
+        assert np.array_equal(slot[:k].cpu().numpy(), ref_dst)
+        assert np.array_equal(s[:k].cpu().numpy(), ref_src)
+
+
+def test_filter_256_pages_to_64(cuda_device):
+    """The 6.3 log line: 256 pages -> 64 per rank at DCP=4."""
+    vals = torch.arange(256, dtype=torch.int32, device=cuda_device)
+    for d in range(4):
+        _, _, cnt = dcp.filter_page_indices(vals, 4, d)
+        assert int(cnt.item()) == 64
+
+
+# --------------------------------------------------------------------------- reshard
+def _reshard_both(case, only_src=-1, only_dst=-1):
+    err = torch.zeros(1, dtype=torch.int32, device=case.src_pools[0].device)
+    before = [p.cpu().view(torch.uint8).numpy().reshape(-1).copy() for p in case.dst_pools]
+    dcp.reshard_pages(case.req_page_ptr, case.src_pages, case.dst_vpages, case.n_layers, case.src_pools,
+                      case.src_pool_pages, case.dst_pools, case.dst_slots, n_dcp=case.n_dcp,
+                      only_src_rank=only_src, only_dst_rank=only_dst, dev_error=err)
+    torch.cuda.synchronize()
+    gpu = [p.cpu().view(torch.uint8).numpy().reshape(-1) for p in case.dst_pools]
+    src = [p.cpu().view(torch.uint8).numpy().reshape(-1).copy() for p in case.src_pools]
+    ref = before
+    st = oracle.reshard(case.req_page_ptr.cpu().numpy(), case.src_pages.cpu().numpy(),
+                        case.dst_vpages.cpu().numpy(), case.page_bytes, case.n_layers, src,
+                        case.src_pool_pages, case.n_dcp, ref, case.dst_slots, only_src, only_dst)
+    assert st == 0
+    return gpu, ref, int(err.item())
+
+
+def _counts(n_layers, n_cp):
+    return [e - s for s, e in (oracle.layer_range(n_layers, n_cp, r) for r in range(n_cp))]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("lens,n_layers,n_cp,n_dcp,contig", [
+    ([1024], 1, 1, 4, False),                      # tiny: 16 pages, 1 source shard, DCP=4
+    ([3000, 64, 700, 129, 5000], 8, 4, 8, True),   # CP4 layer-split -> DCP8, ragged lengths
+    ([640, 200], 5, 3, 3, False),                  # uneven layer split, odd N
+    ([300], 2, 2, 1, True),                        # DCP=1: identity filter
+])
+def test_reshard_bit_exact(cuda_device, dtype, lens, n_layers, n_cp, n_dcp, contig):
+    case = di.reshard_case(lens, n_layers, _counts(n_layers, n_cp), n_dcp, dtype, contig, seed=len(lens),
+                           device=cuda_device, dst_slots=None)
+    gpu, ref, err = _reshard_both(case)
+    assert err == 0
+    for a, b in zip(gpu, ref):
+        assert np.array_equal(a, b)
+
+
+def test_reshard_single_paths_compose(cuda_device):
+    case = di.reshard_case([2000, 900], 6, _counts(6, 3), 4, "e4m3", True, seed=5, device=cuda_device)
+    for r in range(3):
+        for d in range(4):
+            gpu, ref, err = _reshard_both(case, only_src=r, only_dst=d)
+            assert err == 0
+            for a, b in zip(gpu, ref):
+                assert np.array_equal(a, b)
+    full = [p.clone() for p in case.dst_pools]
+    fresh = di.reshard_case([2000, 900], 6, _counts(6, 3), 4, "e4m3", True, seed=5, device=cuda_device)
+    _reshard_both(fresh)
+    for a, b in zip(full, fresh.dst_pools):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+
+
+def test_reshard_out_of_range_sets_device_error(cuda_device):
+    case = di.reshard_case([256], 1, [1], 4, "bf16", True, seed=3, device=cuda_device)
+    case.dst_vpages[1] = case.dst_slots * 4 + 1   # slot past the pool
+    gpu, ref, err = _reshard_both(case)
+    assert err & dcp.DEVERR_OUT_OF_RANGE
+    for a, b in zip(gpu, ref):
+        assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------------- attention
+def _run_attention(case):
+    err = torch.zeros(1, dtype=torch.int32, device=case.q.device)
+    o, l = dcp.partial_decode_attn(case.q, case.seq_lens, case.req_page_ptr, case.dst_vpages, case.pools,
+                                   case.softmax_scale, case.kv_scale, dev_error=err)
+    om, lm = dcp.lse_merge(o, l)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    return o.cpu().numpy(), l.cpu().numpy(), om.cpu().numpy(), lm.cpu().numpy()
+
+
+def _check_all(case, o, l, om, lm):
+    qb, pools = q_bits(case), pool_bytes(case)
+    R = case.rows
+    for d in range(case.n_dcp):
+        ro, rl = oracle_attention(case, rank=d, qb=qb, pools=pools)
+        compare(o[d].reshape(R, 512), l[d].reshape(R), ro, rl, f"{case.name} rank {d}")
+    ro, rl = oracle_attention(case, qb=qb, pools=pools)
+    return compare(om.reshape(R, 512), lm.reshape(R), ro, rl, f"{case.name} merged")
+
+
+ATTN_CASES = [
+    # name, lens, H, T, N, dtype
+    ("tiny", [1024], 16, 1, 4, "bf16"),
+    ("ragged", [1000, 130, 64 * 9 + 5], 64, 1, 4, "bf16"),
+    ("empty-ranks", [64, 200, 1], 64, 1, 8, "bf16"),
+    ("causal-q4", [64 * 7 + 3, 66, 260], 64, 4, 2, "bf16"),
+    ("heads-96", [700, 333], 96, 1, 3, "bf16"),
+    ("dcp1", [1500], 64, 1, 1, "bf16"),
+]
+
+
+@pytest.mark.parametrize("name,lens,H,T,N,dtype", ATTN_CASES, ids=[c[0] for c in ATTN_CASES])
+def test_attention_matches_oracle(cuda_device, name, lens, H, T, N, dtype):
+    case = di.attention_case(lens, H=H, T=T, n_dcp=N, dtype=dtype, slots_per_rank=None, seed=len(name),
+                             device=cuda_device, name=name)
+    _check_all(case, *_run_attention(case))
+
+
+def test_attention_multi_chunk_combine(cuda_device):
+    """A long single request splits into many chunks per rank (in-call chunk merge)."""
+    case = di.attention_case([64 * 1024 + 17], H=64, T=1, n_dcp=2, dtype="bf16", slots_per_rank=None,
+                             seed=21, device=cuda_device, name="long-chunked")
+    o, l, om, lm = _run_attention(case)
+    rows = np.arange(0, 64, 7)
+    qb, pools = q_bits(case), pool_bytes(case)
+    for d in range(2):
+        ro, rl = oracle_attention(case, rank=d, rows=rows, qb=qb, pools=pools)
+        compare(o[d].reshape(64, 512)[rows], l[d].reshape(64)[rows], ro, rl, f"chunked rank {d}")
+    ro, rl = oracle_attention(case, rows=rows, qb=qb, pools=pools)
+    compare(om.reshape(64, 512)[rows], lm.reshape(64)[rows], ro, rl, "chunked merged")
+
+
+def test_attention_batch_full_size_sampled(cuda_device):
+    """32 x 8192 tokens, 64 heads, BF16, DCP=8 at full size; sampled rows vs the oracle."""
+    case = di.batch_case(cuda_device)
+    o, l, om, lm = _run_attention(case)
+    rng = np.random.default_rng(0)
+    rows = np.sort(rng.choice(case.rows, 48, replace=False))
+    qb, pools = q_bits(case), pool_bytes(case)
+    for d in (0, 5):
+        ro, rl = oracle_attention(case, rank=d, rows=rows, qb=qb, pools=pools)
+        compare(o[d].reshape(-1, 512)[rows], l[d].reshape(-1)[rows], ro, rl, f"batch rank {d}")
+    ro, rl = oracle_attention(case, rows=rows, qb=qb, pools=pools)
+    compare(om.reshape(-1, 512)[rows], lm.reshape(-1)[rows], ro, rl, "batch merged")
