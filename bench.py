@@ -35,7 +35,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for the
 # kernels below on the default workload, with the hash of the kernel source they were taken
 # on; a changed source reports traffic null until it is re-measured.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # (kernel, workload): (source hash, bytes per launch); profiles/attn_kernel__batch-32x8192-h64-bf16-dcp8.md
+    ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("37f38495550d4afc", 551839000),
+    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("49a82f8ae989d93b", 331932928),
+}
 
 
 def _src_hash(name: str) -> str:

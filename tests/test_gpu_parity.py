@@ -56,7 +56,7 @@ def test_filter_256_pages_to_64(cuda_device):
 
 
 # --------------------------------------------------------------------------- reshard
-def _reshard_both(case, only_src=-1, only_dst=-1):
+def _reshard_both(case, only_src=-1, only_dst=-1, expect_status=0):
     err = torch.zeros(1, dtype=torch.int32, device=case.src_pools[0].device)
     before = [p.cpu().view(torch.uint8).numpy().reshape(-1).copy() for p in case.dst_pools]
     dcp.reshard_pages(case.req_page_ptr, case.src_pages, case.dst_vpages, case.n_layers, case.src_pools,
@@ -69,7 +69,7 @@ def _reshard_both(case, only_src=-1, only_dst=-1):
     st = oracle.reshard(case.req_page_ptr.cpu().numpy(), case.src_pages.cpu().numpy(),
                         case.dst_vpages.cpu().numpy(), case.page_bytes, case.n_layers, src,
                         case.src_pool_pages, case.n_dcp, ref, case.dst_slots, only_src, only_dst)
-    assert st == 0
+    assert st == expect_status
     return gpu, ref, int(err.item())
 
 
@@ -111,7 +111,7 @@ def test_reshard_single_paths_compose(cuda_device):
 def test_reshard_out_of_range_sets_device_error(cuda_device):
     case = di.reshard_case([256], 1, [1], 4, "bf16", True, seed=3, device=cuda_device)
     case.dst_vpages[1] = case.dst_slots * 4 + 1   # slot past the pool
-    gpu, ref, err = _reshard_both(case)
+    gpu, ref, err = _reshard_both(case, expect_status=-2)
     assert err & dcp.DEVERR_OUT_OF_RANGE
     for a, b in zip(gpu, ref):
         assert np.array_equal(a, b)
