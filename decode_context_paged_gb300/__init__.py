@@ -65,6 +65,9 @@ def _load():
         lib.dcp_partial_decode_attn.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, f32, i32,
                                                 vp, i64, i32, vp, vp, vp, sz, vp, vp]
         lib.dcp_partial_decode_attn.restype = i32
+        lib.dcp_partial_decode_attn_static.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, f32,
+                                                       i32, vp, i64, i32, vp, vp, vp, vp]
+        lib.dcp_partial_decode_attn_static.restype = i32
         lib.dcp_lse_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp, vp]
         lib.dcp_lse_merge.restype = i32
         _lib = lib
@@ -212,6 +215,39 @@ def partial_decode_attn(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: t
                                            _dptr(workspace, "workspace"), workspace.numel(),
                                            _dptr(dev_error, "dev_error", torch.int32), _stream(stream)),
            "dcp_partial_decode_attn")
+    return o_part, lse_part
+
+
+def partial_decode_attn_static(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: torch.Tensor,
+                               dst_vpages: torch.Tensor, kv_pools: list, softmax_scale: float,
+                               kv_scale: float = 1.0, only_rank: int = -1, o_part: torch.Tensor | None = None,
+                               lse_part: torch.Tensor | None = None, dev_error: torch.Tensor | None = None,
+                               stream=None):
+    """Same as partial_decode_attn, for callers that cannot allocate device memory: the call
+    uses the library's fixed device scratch array instead of a workspace.  The outputs must be
+    passed in by such callers (they are only allocated here when omitted, for convenience)."""
+    B, T, H, kd = q.shape
+    if kd != K_DIM:
+        raise ValueError("q must be [B][T][H][576]")
+    N = len(kv_pools)
+    slots = kv_pools[0].shape[0]
+    dtype = _kv_code(kv_pools[0])
+    dev = q.device
+    if o_part is None:
+        o_part = torch.empty((N, B, T, H, V_DIM), dtype=torch.float32, device=dev)
+    if lse_part is None:
+        lse_part = torch.empty((N, B, T, H), dtype=torch.float32, device=dev)
+    kp = _ptr_array(kv_pools, "kv_pools")
+    _check(_load().dcp_partial_decode_attn_static(B, T, H, _dptr(q, "q", torch.bfloat16),
+                                                  _dptr(seq_lens, "seq_lens", torch.int32),
+                                                  _dptr(req_page_ptr, "req_page_ptr", torch.int64),
+                                                  dst_vpages.numel(), _dptr(dst_vpages, "dst_vpages", torch.int32),
+                                                  PAGE, dtype, float(kv_scale), float(softmax_scale), N,
+                                                  ctypes.addressof(kp), slots, only_rank,
+                                                  _dptr(o_part, "o_part", torch.float32),
+                                                  _dptr(lse_part, "lse_part", torch.float32),
+                                                  _dptr(dev_error, "dev_error", torch.int32), _stream(stream)),
+           "dcp_partial_decode_attn_static")
     return o_part, lse_part
 
 

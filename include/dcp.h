@@ -172,6 +172,36 @@ int dcp_partial_decode_attn(int num_requests, int q_len, int num_heads, const vo
                             size_t workspace_bytes, int32_t *dev_error, dcp_stream_t stream);
 
 /*
+ * Partial attention for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot call cudaMalloc, such
+ * as a host whose pool allocator owns all device memory and hands plug-ins only tensor
+ * pointers, or a decode loop in which an allocation (which may synchronise the device) is
+ * not allowed.  It computes exactly what dcp_partial_decode_attn computes, with the same
+ * arguments except the workspace: the scratch is a fixed device array inside the library of
+ * DCP_STATIC_ATTN_SCRATCH_BYTES, created when the library's device code is loaded and held
+ * by every GPU that loads the library until the process exits.  Nothing is allocated per
+ * call.
+ *   - The first call on a device looks up the array's device address (once per device,
+ *     cached); make that first call before any stream capture.
+ *   - Sizes whose scratch need (dcp_partial_decode_attn_workspace_size for the same
+ *     arguments and dtype) exceeds DCP_STATIC_ATTN_SCRATCH_BYTES return DCP_ERR_WORKSPACE.
+ *   - The array keeps the last call's contents; each call rewrites everything it reads
+ *     (the plan kernels reset the work counter to zero), so nothing needs clearing.
+ *   - All calls share the one array: calls that may overlap on the GPU (other streams or
+ *     host threads without ordering) race on it and must not be issued.
+ * Returns the statuses of dcp_partial_decode_attn, plus DCP_ERR_WORKSPACE for sizes over
+ * the limit.
+ */
+#define DCP_STATIC_ATTN_SCRATCH_BYTES (64u << 20)
+int dcp_partial_decode_attn_static(int num_requests, int q_len, int num_heads, const void *q,
+                                   const int32_t *seq_lens, const int64_t *req_page_ptr,
+                                   int64_t num_pages, const int32_t *dst_vpages, int page_size,
+                                   int dtype, float kv_scale, float softmax_scale, int n_dcp,
+                                   const void *const *kv_pools, int64_t slots_per_rank,
+                                   int only_rank, float *o_part, float *lse_part,
+                                   int32_t *dev_error, dcp_stream_t stream);
+
+/*
  * [P1] 5.2 "All-Gather + LSE Merge" (LSE_merged = log sum_d exp LSE_d) and [P2] (exact
  * recombination): per row r, M = max_d LSE_d, w_d = exp(LSE_d - M),
  *     LSE[r] = M + ln sum_d w_d,   O[r] = sum_d w_d O_d[r] / sum_d w_d,
