@@ -114,27 +114,41 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------ workload
-class Workload:
-    """The default batch workload, resident in HBM, plus its per-step algorithmic sizes."""
+WORKLOADS = {
+    # name: (lengths, heads, q_len, DCP ranks, KV dtype, layers, CP source ranks, slots per rank)
+    "tiny": (lambda: [1024], 16, 1, 4, "bf16", 1, 1, 4),
+    "batch": (lambda: [8192] * 32, 64, 1, 8, "bf16", 1, 1, 512),
+    "agent": (lambda: [100_000] * 48, 64, 1, 8, "e4m3", 1, 1, 9408),
+    "long": (lambda: [1 << 20] * 4, 64, 4, 8, "e4m3", 1, 1, 8192),
+    "e2e": (lambda: di.e2e_lengths(), 64, 1, 8, "e4m3", di.E2E_LAYERS, di.E2E_NCP, None),
+}
 
-    def __init__(self, device, seed: int = 1):
-        self.B, self.T, self.H, self.N = 32, 1, 64, 8
-        self.n_tokens = 8192
-        self.dtype = "bf16"
-        lens = [self.n_tokens] * self.B
-        self.rc = di.reshard_case(lens, n_layers=1, layer_counts=[1], n_dcp=self.N, dtype=self.dtype,
-                                  contiguous_src=True, seed=seed, device=device, dst_slots=512)
+
+class Workload:
+    """One workload resident in HBM (source pools, destination pools, Q, outputs) plus its
+    per-step algorithmic bytes.  A step = reshard all layers, then per layer partial attention
+    on every DCP rank and the LSE merge."""
+
+    def __init__(self, name: str, device, seed: int = 1):
+        import decode_context_paged_gb300 as dcp
+        lens_fn, self.H, self.T, self.N, self.dtype, self.L, self.n_cp, slots = WORKLOADS[name]
+        lens = lens_fn()
+        self.lens = lens
+        self.B = len(lens)
+        counts = [e - s for s, e in (dcp.layer_range(self.L, self.n_cp, r) for r in range(self.n_cp))]
+        self.rc = di.reshard_case(lens, n_layers=self.L, layer_counts=counts, n_dcp=self.N, dtype=self.dtype,
+                                  contiguous_src=True, seed=seed, device=device, dst_slots=slots)
         self.q = di.random_q(self.B, self.T, self.H, di._gen(seed + 7, device), device)
         self.seq_lens = torch.tensor(lens, dtype=torch.int32, device=device)
-        self.pools = [p[0] for p in self.rc.dst_pools]
-        self.kv_scale = 1.0
+        self.layer_pools = [[p[l] for p in self.rc.dst_pools] for l in range(self.L)]
+        self.kv_scale = di.FP8_KV_SCALE if self.dtype == "e4m3" else 1.0
         self.scale = di.SOFTMAX_SCALE
         R = self.B * self.T * self.H
+        self.R = R
         self.o_part = torch.empty((self.N, self.B, self.T, self.H, 512), dtype=torch.float32, device=device)
         self.lse_part = torch.empty((self.N, self.B, self.T, self.H), dtype=torch.float32, device=device)
-        self.o = torch.empty((self.B, self.T, self.H, 512), dtype=torch.float32, device=device)
-        self.lse = torch.empty((self.B, self.T, self.H), dtype=torch.float32, device=device)
-        import decode_context_paged_gb300 as dcp
+        self.o = torch.empty((self.L, self.B, self.T, self.H, 512), dtype=torch.float32, device=device)
+        self.lse = torch.empty((self.L, self.B, self.T, self.H), dtype=torch.float32, device=device)
         self.ws = dcp.alloc_workspace(self.B, self.T, self.H, self.N, self.rc.dst_vpages.numel(), device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         pages = self.rc.dst_vpages.numel()
@@ -142,32 +156,40 @@ class Workload:
         page_bytes = 64 * 576 * elem
         tokens = sum(lens)
         self.bytes = {
-            "reshard": 2 * pages * page_bytes,                       # read + write every page
-            "attn": tokens * 576 * elem + self.q.numel() * 2 + self.N * R * (512 + 1) * 4,
-            "merge": self.N * R * (512 + 1) * 4 + R * (512 + 1) * 4,
+            "reshard": 2 * pages * page_bytes * self.L,              # read + write every page of every layer
+            "attn": self.L * (tokens * 576 * elem + self.q.numel() * 2 + self.N * R * (512 + 1) * 4),
+            "merge": self.L * (self.N * R * (512 + 1) * 4 + R * (512 + 1) * 4),
         }
-        self.flops_attn = 2 * tokens * self.T * self.H * (576 + 512)
-        self.name = f"batch-{self.B}x{self.n_tokens}-h{self.H}-q{self.T}-{self.dtype}-dcp{self.N}"
+        keys = sum(sum(n - self.T + t + 1 for t in range(self.T)) for n in lens)  # visible (row, key) per head
+        self.flops_attn = 2 * keys * self.H * (576 + 512) * self.L
+        self.name = (f"{name}-{self.B}x{max(lens)}-h{self.H}-q{self.T}-{self.dtype}-dcp{self.N}"
+                     + (f"-L{self.L}-cp{self.n_cp}" if self.L > 1 else ""))
+        self.launches_per_step = 1 + self.L * (6 if self.dtype == "e4m3" else 5)
 
     def step(self, dcp, events=None):
+        """events: dict stage -> list of (start, end) event pairs, appended per call."""
         rc = self.rc
-        if events:
-            events[0].record()
-        dcp.reshard_pages(rc.req_page_ptr, rc.src_pages, rc.dst_vpages, 1, rc.src_pools, rc.src_pool_pages,
-                          rc.dst_pools, rc.dst_slots, dev_error=self.err)
-        if events:
-            events[1].record()
-        dcp.partial_decode_attn(self.q, self.seq_lens, rc.req_page_ptr, rc.dst_vpages, self.pools, self.scale,
-                                self.kv_scale, o_part=self.o_part, lse_part=self.lse_part, workspace=self.ws,
-                                dev_error=self.err)
-        if events:
-            events[2].record()
-        dcp.lse_merge(self.o_part, self.lse_part, self.o, self.lse)
-        if events:
-            events[3].record()
+
+        def rec(stage, fn):
+            if events is None:
+                fn()
+                return
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            events.setdefault(stage, []).append((a, b))
+
+        rec("reshard", lambda: dcp.reshard_pages(rc.req_page_ptr, rc.src_pages, rc.dst_vpages, self.L, rc.src_pools,
+                                                 rc.src_pool_pages, rc.dst_pools, rc.dst_slots, dev_error=self.err))
+        for l in range(self.L):
+            rec("attn", lambda: dcp.partial_decode_attn(self.q, self.seq_lens, rc.req_page_ptr, rc.dst_vpages,
+                                                        self.layer_pools[l], self.scale, self.kv_scale,
+                                                        o_part=self.o_part, lse_part=self.lse_part, workspace=self.ws,
+                                                        dev_error=self.err))
+            rec("merge", lambda: dcp.lse_merge(self.o_part, self.lse_part, self.o[l], self.lse[l]))
 
 
-LAUNCHES_PER_STEP = 6  # reshard, plan pages, plan units, attention, chunk combine, merge
 
 
 def dist_setup():
@@ -197,8 +219,10 @@ def max_over_ranks(dist, x: float) -> float:
 
 # ------------------------------------------------------------------------- CPU oracle leg
 def oracle_sample(wl, max_seconds: float = 20.0):
-    """Times the float64 oracle on a bounded sample of the workload: whole requests (their
-    reshard, per-rank partial attention and merge), adding requests until ~max_seconds."""
+    """Times the float64 oracle on a bounded sample of the workload: request by request, the
+    reshard of the request's pages (every layer), then for layer 0 the per-rank partial
+    attention and merge of a subset of the request's query rows, until ~max_seconds.
+    Returns GB/s over the sample's share of the step's algorithmic bytes."""
     import numpy as np
 
     import oracle
@@ -209,25 +233,40 @@ def oracle_sample(wl, max_seconds: float = 20.0):
     vp = rc.dst_vpages.cpu().numpy()
     src = [p.cpu().view(torch.uint8).numpy().reshape(-1) for p in rc.src_pools]
     qb = wl.q.cpu().view(torch.int16).numpy().view(np.uint16)
-    per_req_bytes = sum(wl.bytes.values()) / wl.B
-    done, t_total = 0, 0.0
-    while done < wl.B and t_total < max_seconds:
-        b = done
+    dt = oracle.BF16 if wl.dtype == "bf16" else oracle.E4M3
+    pages_total = len(vp)
+    rows_per_req = wl.T * wl.H
+    step_rows = wl.B * rows_per_req * wl.L
+    attn_merge = wl.bytes["attn"] + wl.bytes["merge"]
+    done_bytes, t_total, n_req, n_rows = 0.0, 0.0, 0, 0
+    b = 0
+    while t_total < max_seconds and b < wl.B:
         p0, p1 = int(ptr[b]), int(ptr[b + 1])
         sub_ptr = np.array([0, p1 - p0], np.int64)
-        dst = [np.zeros(rc.dst_slots * rc.page_bytes, np.uint8) for _ in range(wl.N)]
+        # rows: all of them when the request is short, fewer for long contexts
+        keys = wl.lens[b]
+        n_sel = max(1, min(rows_per_req, int(4e9 / (keys * 2176 * 2))))
+        rows = np.arange(n_sel, dtype=np.int64) * max(1, rows_per_req // n_sel)
+        dst = [np.zeros(wl.L * rc.dst_slots * rc.page_bytes, np.uint8) for _ in range(wl.N)]
         t0 = time.perf_counter()
-        oracle.reshard(sub_ptr, src_pages[p0:p1], vp[p0:p1], rc.page_bytes, 1, src, rc.src_pool_pages, wl.N,
+        oracle.reshard(sub_ptr, src_pages[p0:p1], vp[p0:p1], rc.page_bytes, wl.L, src, rc.src_pool_pages, wl.N,
                        dst, rc.dst_slots)
-        pools = [d.view(np.uint16).reshape(rc.dst_slots, 64, 576) for d in dst]
-        parts = [oracle.attention(qb[b:b + 1], np.array([wl.n_tokens], np.int32), sub_ptr, vp[p0:p1], pools,
-                                  oracle.BF16, 1.0, wl.scale, wl.N, rank=d, q_len=wl.T, num_heads=wl.H)
+        esz = 2 if wl.dtype == "bf16" else 1
+        pools = [d.reshape(wl.L, rc.dst_slots * 64 * 576 * esz)[0].view(np.uint16 if esz == 2 else np.uint8)
+                 .reshape(rc.dst_slots, 64, 576) for d in dst]
+        parts = [oracle.attention(qb[b:b + 1], np.array([wl.lens[b]], np.int32), sub_ptr, vp[p0:p1], pools,
+                                  dt, wl.kv_scale, wl.scale, wl.N, rank=d, rows=rows, q_len=wl.T, num_heads=wl.H)
                  for d in range(wl.N)]
         oracle.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
         t_total += time.perf_counter() - t0
-        done += 1
-    gbs = done * per_req_bytes / t_total / 1e9
-    return gbs, done, t_total, oracle.num_threads()
+        done_bytes += wl.bytes["reshard"] * (p1 - p0) / pages_total + attn_merge * len(rows) / step_rows
+        n_req += 1
+        n_rows += len(rows)
+        b += 1
+    gbs = done_bytes / t_total / 1e9
+    desc = (f"{n_req} of {wl.B} requests: reshard of their pages ({wl.L} layers) + layer-0 partial attention "
+            f"over {wl.N} ranks and merge for {n_rows} of their {n_req * rows_per_req} query rows; {t_total:.1f} s")
+    return gbs, desc, t_total, oracle.num_threads()
 
 
 # ------------------------------------------------------------------------------- main
@@ -236,27 +275,26 @@ def run_reference(args):
     if rank != 0:
         return
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
-    wl = Workload(dev)
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm state; warm-up steps are not needed for a CPU program
-    vals = []
-    samples = []
-    for _ in range(args.steps):
-        gbs, done, secs, threads = oracle_sample(wl, max_seconds=args.ref_seconds)
+    wl = Workload(args.config, dev)
+    vals, secs, desc, threads = [], [], "", 1
+    for _ in range(args.steps):  # the oracle has no warm state: warm-up steps are not run
+        gbs, desc, t, threads = oracle_sample(wl, max_seconds=args.ref_seconds)
         vals.append(gbs)
-        samples.append((done, secs))
+        secs.append(t)
     v = statistics.median(vals)
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": 1e3 * sum(s for _, s in samples) / max(1, args.steps),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": wl.name, "l2": "inputs larger than L2"},
-        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{samples[0][0]} of {wl.B} requests per step (reshard + {wl.N} partials + merge)"},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def _stage_ms(events, steps):
+    return {k: sum(a.elapsed_time(b) for a, b in v) / steps for k, v in events.items()}
 
 
 def run_ours(args):
@@ -264,7 +302,7 @@ def run_ours(args):
     dist, rank, world, local = dist_setup()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = Workload(dev, seed=1 + rank)
+    wl = Workload(args.config, dev, seed=1 + rank)
     stream = torch.cuda.current_stream()
 
     for _ in range(max(args.warmup, 3)):
@@ -273,30 +311,27 @@ def run_ours(args):
     if int(wl.err.item()) != 0:
         raise RuntimeError(f"device error word {int(wl.err.item())}")
 
-    # ---- timed region: K steps, per-stage events on the launching stream
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    # ---- timed region: K steps, per-stage CUDA events on the launching stream
+    events = {}
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(dist)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         start.record(stream)
-        for k in range(args.steps):
-            wl.step(dcp, ev[k])
+        for _ in range(args.steps):
+            wl.step(dcp, events)
         end.record(stream)
         torch.cuda.synchronize()
     barrier(dist)
-    ms = start.elapsed_time(end)
-    ms = max_over_ranks(dist, ms)
-    stage_ms = {
-        "reshard": sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps,
-        "attn": sum(e[1].elapsed_time(e[2]) for e in ev) / args.steps,
-        "merge": sum(e[2].elapsed_time(e[3]) for e in ev) / args.steps,
-    }
+    ms = max_over_ranks(dist, start.elapsed_time(end))
+    stage_ms = _stage_ms(events, args.steps)
     step_bytes = sum(wl.bytes.values())
     ms_step = ms / args.steps
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    if int(wl.err.item()) != 0:
+        raise RuntimeError(f"device error word {int(wl.err.item())}")
 
-    # ---- end to end through the public API with host buffers
+    # ---- end to end through the public API with host buffers (pinned)
     host_src = [p.cpu().pin_memory() for p in wl.rc.src_pools]
     host_q = wl.q.cpu().pin_memory()
     host_o = torch.empty(wl.o.shape, dtype=torch.float32).pin_memory()
@@ -317,12 +352,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier(dist)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 10))
     e0.record(stream)
-    for _ in range(args.steps):
+    for _ in range(e2e_steps):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1)) / args.steps
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1)) / e2e_steps
     e2e_value = world * step_bytes / (e2e_ms * 1e-3) / 1e9
 
     if rank != 0:
@@ -335,31 +371,43 @@ def run_ours(args):
     src_of = {"reshard": "dcp_reshard.cu", "attn": "dcp_attn.cu", "merge": "dcp_merge.cu"}
     tr = NCU_TRAFFIC.get((kernel_of[dom], wl.name))
     traffic = tr[1] if tr and tr[0] == _src_hash(src_of[dom]) else None
-    roof = {"kernel": kernel_of[dom], "bound": "hbm", "achieved": stage_gbs[dom], "peak": hbm, "unit": "GB/s",
-            "frac": stage_gbs[dom] / hbm, "peak_kind": peak_kind, "traffic": traffic,
-            "algorithmic_bytes": wl.bytes[dom]}
+    # the tensor roofline uses the peak of the MMA kind executed (kind::f8f6f4 = 2x the BF16 rate)
+    tc_peak = bf16 * (2.0 if wl.dtype == "e4m3" else 1.0)
+    attn_bound = "tensor" if wl.flops_attn / tc_peak / 1e12 > wl.bytes["attn"] / hbm / 1e9 else "hbm"
+    if dom == "attn" and attn_bound == "tensor":
+        roof = {"kernel": "attn_kernel", "bound": "tensor", "achieved": attn_tflops, "peak": tc_peak,
+                "unit": "TFLOP/s", "frac": attn_tflops / tc_peak, "peak_kind": peak_kind + (
+                    " bf16 x2 for kind::f8f6f4" if wl.dtype == "e4m3" else " bf16"),
+                "traffic": traffic, "algorithmic_flops": wl.flops_attn}
+    else:
+        roof = {"kernel": kernel_of[dom], "bound": "hbm", "achieved": stage_gbs[dom], "peak": hbm, "unit": "GB/s",
+                "frac": stage_gbs[dom] / hbm, "peak_kind": peak_kind, "traffic": traffic,
+                "algorithmic_bytes": wl.bytes[dom]}
     cpu = None
     if not args.no_cpu_baseline:
-        gbs, done, secs, threads = oracle_sample(wl, max_seconds=args.ref_seconds)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{done} of {wl.B} requests (reshard + {wl.N} partials + merge), {secs:.1f} s"}
+        gbs, desc, secs, threads = oracle_sample(wl, max_seconds=args.ref_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "l2": "inputs larger than L2 (302 MB pools)",
-                   "bytes_per_step": step_bytes, "parallelism": f"replicas x{world}"},
+        "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "e4m3 (fp32 accumulate)",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "l2": "inputs larger than L2", "bytes_per_step": step_bytes,
+                   "parallelism": f"replicas x{world}"},
         "stages": {
             "reshard": {"ms": stage_ms["reshard"], "GB/s": stage_gbs["reshard"], "frac_hbm": stage_gbs["reshard"] / hbm},
             "attn": {"ms": stage_ms["attn"], "GB/s": stage_gbs["attn"], "TFLOP/s": attn_tflops,
-                     "frac_hbm": stage_gbs["attn"] / hbm, "frac_bf16": attn_tflops / bf16},
+                     "frac_hbm": stage_gbs["attn"] / hbm, "frac_tensor": attn_tflops / tc_peak, "bound": attn_bound},
             "merge": {"ms": stage_ms["merge"], "GB/s": stage_gbs["merge"], "frac_hbm": stage_gbs["merge"] / hbm},
+            "attn_plus_merge_frac_of_roofline": (
+                max((wl.bytes["attn"] + wl.bytes["merge"]) / hbm / 1e9, wl.flops_attn / tc_peak / 1e12)
+                / ((stage_ms["attn"] + stage_ms["merge"]) * 1e-3)),
         },
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
     print(json.dumps(line), flush=True)
@@ -371,6 +419,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=sorted(WORKLOADS), default="batch")
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -12,28 +12,35 @@
 //    request, chunk, query group), a query group being one new token and up to 64 heads.
 //    Units are ordered by size (largest first) with the groups of one chunk adjacent, and
 //    persistent CTAs (one per SM) take them from an atomic counter.
-//  * Per tile, tcgen05 computes S^T[128 tokens x 64 query rows] = K_tile * Q^T (K-major
-//    BF16 operands, 128-byte swizzle, FP32 accumulator in TMEM, M = 128 tokens so the
-//    whole tensor datapath is used), then O^T[512 x 64] += V_tile^T * P^T (V read MN-major
-//    from the same page rows, P written by the softmax warps).  O^T (256 TMEM columns) and
-//    two S buffers (64 columns each) fit in one 512-column allocation.
-//  * TMA streams 64-row x 64-dim boxes of the page pool into an 8-slot ring of 16 KB blocks
-//    (two pages per block): the nine 64-dim blocks of a tile for S, then the eight V blocks
-//    again (they come back from L2) for P*V, so the ring never has to hold a whole tile.
-//  * Four softmax warps own one token row each (TMEM lane = row): scores are masked
-//    (ragged last page, causal limit among the new tokens), column maxima are reduced with
-//    a warp-shuffle reduce-scatter plus shared memory, exp2 weights go to shared memory as
-//    BF16 P^T, and O^T is rescaled in TMEM only when a column's running max moved.
+//  * Tokens are the MMA's M dimension (128 = two pages), query rows its N.  Per tile
+//    tcgen05 computes S^T[128 x n] = K_tile * Q^T into TMEM, the softmax warps turn it into
+//    P^T in shared memory, and tcgen05 accumulates O^T[512 x 64] += V_tile^T * P^T in TMEM.
+//    BF16 pools use kind::f16 (BF16 operands).  FP8-E4M3 pools use kind::f8f6f4 on the raw
+//    page bytes: Q enters as two E4M3 terms (hi + lo, stacked as N = 128 rows, with a
+//    power-of-two scale per query row) so the scores keep BF16-level accuracy, and P enters
+//    as hi + lo terms accumulated into the same O^T.
+//  * Two TMA streams: the K stream (all 576 dims of a tile, read from HBM with an L2
+//    evict-last hint) feeds the score MMAs through a 4-slot ring; the V stream re-reads the
+//    512 latent dims of the same pages (an L2 hit) into a 2-unit ring for P*V.  Separate
+//    MMA-issuing threads for the two products keep HBM loads in flight while the softmax
+//    of an earlier tile runs.
+//  * Eight softmax warps (two warpgroups of 32 query columns each) own one token row per
+//    thread (TMEM lane = row): scores are masked
+//    (ragged last page, causal limit among the new tokens), column maxima are reduced with a
+//    warp-shuffle reduce-scatter plus shared memory, exp2 weights go to shared memory, and
+//    O^T is rescaled in TMEM only when a column's running max moved.
 //  * Single-chunk segments write O_part / LSE_part directly; multi-chunk segments write
 //    chunk partials to the workspace and a combine kernel merges them (exact LSE merge).
 //  * Every mbarrier wait is bounded; on timeout the CTA stops, drains its in-flight copies
 //    and MMAs, frees TMEM and reports DCP_DEVERR_TIMEOUT.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
 #include <cmath>
+#include <cstring>
 
 #include "dcp_internal.h"
 #include "dcp_merge_row.cuh"
@@ -42,23 +49,32 @@
 namespace dcp {
 namespace {
 
-constexpr int kRingSlots = 8;
-constexpr uint32_t kBlockBytes = 16384;  // 128 token rows x 64 dims x 2 bytes
-constexpr uint32_t kHalfBlock = 8192;    // one page (64 rows) x 64 dims
-constexpr int kQBlocks = 9;              // 576 / 64
-constexpr int kVBlocks = 8;              // 512 / 64
-constexpr uint32_t kQBytes = kQBlocks * kHalfBlock;
-constexpr uint32_t kPBytes = 16384;      // 128 tokens x 64 query rows x 2 bytes
+constexpr int kKSlots = 4;               // K-stream ring: 16 KB slots
+constexpr int kVSlots = 2;               // V-stream ring: 32 KB units
+constexpr uint32_t kKSlotBytes = 16384;
+constexpr uint32_t kVSlotBytes = 32768;
+constexpr uint32_t kQBytes = 73728;      // 64 rows x 576 BF16, or 128 rows (hi, lo) x 576 E4M3
+constexpr uint32_t kPBytes = 16384;
 constexpr int kGroupRows = 64;
-constexpr uint32_t kOffQ = kRingSlots * kBlockBytes;
+constexpr uint32_t kOffV = kKSlots * kKSlotBytes;
+constexpr uint32_t kOffQ = kOffV + kVSlots * kVSlotBytes;
 constexpr uint32_t kOffP = kOffQ + kQBytes;
 constexpr uint32_t kOffCtl = kOffP + kPBytes;
-constexpr int kThreads = 192;            // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kThreads = 384;            // 0 K-TMA, 1 S-MMA, 2 V-TMA, 3 PV-MMA, 4-11 softmax
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = 256;          // S buffers at TMEM columns 256 and 320
-constexpr uint32_t kIdescS = idesc_bf16_f32(128, 64, 0, 0);
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 64, 1, 1);
+constexpr uint32_t kSCol = 256;          // S buffers start at TMEM column 256 (O^T uses 0..255)
 constexpr int kMaxTpc = 4096;
+constexpr float kPScale = 256.f;         // FP8 P is stored as 256 * p (E4M3 range 448)
+
+template <bool F8>
+struct Cfg {
+    static constexpr int kKBlocks = F8 ? 5 : 9;     // K-stream blocks per tile
+    static constexpr int kVUnits = F8 ? 2 : 4;      // V-stream units per tile
+    static constexpr int kSCols = F8 ? 128 : 64;    // TMEM columns per S buffer (hi, lo for FP8)
+    static constexpr int kSBufs = F8 ? 2 : 3;
+    static constexpr uint32_t kIdescS = F8 ? idesc_e4m3_f32(128, 128, 0, 0) : idesc_bf16_f32(128, 64, 0, 0);
+    static constexpr uint32_t kIdescPV = F8 ? idesc_e4m3_f32(128, 64, 1, 1) : idesc_bf16_f32(128, 64, 1, 1);
+};
 
 struct UnitInfo {
     int valid, d, b, g;
@@ -68,16 +84,18 @@ struct UnitInfo {
 };
 
 struct __align__(16) Ctl {
-    float red[4][64];
+    float red[2][4][32];
     float m_run[64];
     float corr[64];
     float oscale[64];
-    uint64_t full[kRingSlots], empty[kRingSlots];
+    float qscale[64];            // per query row: softmax_scale * kappa * log2(e) * 2^-qexp
+    uint64_t kfull[kKSlots], kempty[kKSlots];
+    uint64_t vfull[kVSlots], vempty[kVSlots];
     uint64_t q_full, q_empty;
-    uint64_t s_full[2], s_free[2];
+    uint64_t s_full[3], s_free[3];
     uint64_t p_full, o_done, o_free;
     uint64_t unit_full[2], unit_empty[2];
-    uint64_t drain;
+    uint64_t drain_s, drain_pv;
     UnitInfo unit[2];
     uint32_t tmem_base;
     int abort_flag;
@@ -86,8 +104,8 @@ constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(Ctl);
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct AttnMaps {
-    CUtensorMap q;
-    CUtensorMap kv[kMaxDcpAttn];
+    CUtensorMap q[2];                  // BF16: [0] 64x64 boxes.  FP8 (hi|lo rows): [0] 128x64 SW128, [1] 64x64 SW64
+    CUtensorMap kv[kMaxDcpAttn][2];    // same split per pool
 };
 
 struct KParams {
@@ -95,42 +113,44 @@ struct KParams {
     const int64_t *req_page_ptr;
     const int32_t *comp_slot;  // [N][num_pages]: rank d's pages of request b start at d*num_pages + ptr[b]
     const int32_t *comp_page;  // page index j (within the request) of each compacted entry
-    const int4 *units;         // {pair, page_begin, n_pages, out_index}, pair = d*B + b ... see plan
+    const int4 *units;         // {pair*G + g, page_begin, n_pages, out_index}
     const int *ctrl;           // [0] = number of units, [1] = work counter
     int *counter;
-    int B, T, H, HB, G;
+    const float *q_rscale;     // FP8: 2^-qexp per query row
+    int B, T, H, HB, G, R;
     long long num_pages;
     int oob_row;               // a TMA row coordinate past the pool (zero fill)
     float sl2;                 // softmax_scale * kappa * log2(e)
-    float kv_scale;            // kappa applied to V
+    float out_scale;           // kappa (BF16) or kappa / 256 (FP8) applied to O
     float *o_part, *lse_part, *part_o, *part_lse;
     int32_t *dev_error;
     unsigned long long wait_limit_ns;
 };
 
 // ---------------------------------------------------------------------- warp reductions
-// Reduce-scatter over the warp: on entry each lane holds the 64 column values of its token
-// in v; on exit r[0], r[1] of lane L hold the reduction over the warp's 32 tokens of
-// columns 2L and 2L+1.  62 shuffles instead of 64 x 5 for a plain butterfly.
+// Reduce-scatter over the warp: on entry each lane holds the 32 column values of its token;
+// on exit lane L holds the reduction over the warp's 32 tokens of column L (31 shuffles
+// instead of 32 x 5 for a plain butterfly).
 template <bool kMax>
 __device__ __forceinline__ float rs_op(float a, float b) { return kMax ? fmaxf(a, b) : a + b; }
 
 template <bool kMax>
-__device__ __forceinline__ void reduce_scatter64(const float (&v)[64], float (&r)[32], int lane) {
+__device__ __forceinline__ float reduce_scatter32(const float (&v)[32], int lane) {
+    float r[16];
     {
         const bool upper = (lane & 16) != 0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float send = upper ? v[i] : v[i + 32];
-            const float keep = upper ? v[i + 32] : v[i];
+        for (int i = 0; i < 16; ++i) {
+            const float send = upper ? v[i] : v[i + 16];
+            const float keep = upper ? v[i + 16] : v[i];
             r[i] = rs_op<kMax>(keep, __shfl_xor_sync(0xffffffffu, send, 16));
         }
     }
 #pragma unroll
-    for (int half = 16, off = 8; half >= 2; half >>= 1, off >>= 1) {
+    for (int half = 8, off = 8; half >= 1; half >>= 1, off >>= 1) {
         const bool upper = (lane & off) != 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < 8; ++i) {
             if (i < half) {
                 const float send = upper ? r[i] : r[i + half];
                 const float keep = upper ? r[i + half] : r[i];
@@ -138,6 +158,14 @@ __device__ __forceinline__ void reduce_scatter64(const float (&v)[64], float (&r
             }
         }
     }
+    return r[0];
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22; 2^-inf = 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // Warp-uniform bounded wait: every lane polls, the warp agrees on the outcome.
@@ -152,11 +180,72 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// E4M3 hi/lo split of 4 values (already scaled into range): hi = e4m3(x), lo = e4m3(x - hi).
+__device__ __forceinline__ void split_e4m3x4(float a, float b, float c, float d, uint32_t &hi, uint32_t &lo) {
+    const __nv_fp8x2_storage_t h01 = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t h23 = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    const __half2_raw r01 = __nv_cvt_fp8x2_to_halfraw2(h01, __NV_E4M3);
+    const __half2_raw r23 = __nv_cvt_fp8x2_to_halfraw2(h23, __NV_E4M3);
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2 *>(&r01));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2 *>(&r23));
+    const __nv_fp8x2_storage_t l01 = __nv_cvt_float2_to_fp8x2(make_float2(a - f01.x, b - f01.y), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t l23 = __nv_cvt_float2_to_fp8x2(make_float2(c - f23.x, d - f23.y), __NV_SATFINITE, __NV_E4M3);
+    hi = (uint32_t)h01 | ((uint32_t)h23 << 16);
+    lo = (uint32_t)l01 | ((uint32_t)l23 << 16);
+}
+
+// FP8 path: Q (BF16) -> hi and lo E4M3 rows scaled by a power of two per row so that the
+// row's largest magnitude lands in (224, 448]; q = (hi + lo) * 2^-qexp up to ~2^-8 relative.
+// One warp per query row.  Output rows [0, R) = hi, [R, 2R) = lo; rscale[row] = 2^-qexp.
+__global__ void q_split_kernel(int R, const __nv_bfloat16 *__restrict__ q, uint8_t *__restrict__ qhl,
+                               float *__restrict__ rscale) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= R) return;
+    const __nv_bfloat16 *src = q + (long long)row * kKDim;
+    float v[18];
+#pragma unroll
+    for (int k = 0; k < 9; ++k) {  // lane covers columns 2*(lane + 32k), +1
+        const __nv_bfloat162 x = reinterpret_cast<const __nv_bfloat162 *>(src)[lane + 32 * k];
+        v[2 * k] = __bfloat162float(x.x);
+        v[2 * k + 1] = __bfloat162float(x.y);
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int k = 0; k < 18; ++k) amax = fmaxf(amax, fabsf(v[k]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    int e = 0;
+    if (amax > 0.f) {
+        e = (int)floorf(log2f(448.f / amax));
+        e = max(-100, min(100, e));
+    }
+    const float sc = ldexpf(1.f, e);
+    uint8_t *hi = qhl + (long long)row * kKDim;
+    uint8_t *lo = qhl + ((long long)R + row) * kKDim;
+#pragma unroll
+    for (int k = 0; k < 9; ++k) {
+        const int c = 2 * (lane + 32 * k);
+        const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(make_float2(v[2 * k] * sc, v[2 * k + 1] * sc),
+                                                                __NV_SATFINITE, __NV_E4M3);
+        const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3);
+        const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+        const __nv_fp8x2_storage_t l = __nv_cvt_float2_to_fp8x2(
+            make_float2(v[2 * k] * sc - hf.x, v[2 * k + 1] * sc - hf.y), __NV_SATFINITE, __NV_E4M3);
+        *reinterpret_cast<__nv_fp8x2_storage_t *>(hi + c) = h;
+        *reinterpret_cast<__nv_fp8x2_storage_t *>(lo + c) = l;
+    }
+    if (lane == 0) rscale[row] = ldexpf(1.f, -e);
+}
+
+template <bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KParams p) {
+    using C = Cfg<F8>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *ring = base;
+    uint8_t *kring = base;
+    uint8_t *vring = base + kOffV;
     uint8_t *sq = base + kOffQ;
     uint8_t *sp = base + kOffP;
     Ctl *ctl = reinterpret_cast<Ctl *>(base + kOffCtl);
@@ -165,22 +254,29 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
     const uint64_t lim = p.wait_limit_ns;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kRingSlots; ++i) {
-            mbar_init(&ctl->full[i], 1);
-            mbar_init(&ctl->empty[i], 1);
+        for (int i = 0; i < kKSlots; ++i) {
+            mbar_init(&ctl->kfull[i], 1);
+            mbar_init(&ctl->kempty[i], 1);
+        }
+        for (int i = 0; i < kVSlots; ++i) {
+            mbar_init(&ctl->vfull[i], 1);
+            mbar_init(&ctl->vempty[i], 1);
         }
         mbar_init(&ctl->q_full, 1);
         mbar_init(&ctl->q_empty, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 3; ++i) {
             mbar_init(&ctl->s_full[i], 1);
-            mbar_init(&ctl->s_free[i], 128);
-            mbar_init(&ctl->unit_full[i], 1);
-            mbar_init(&ctl->unit_empty[i], 2);
+            mbar_init(&ctl->s_free[i], 256);
         }
-        mbar_init(&ctl->p_full, 128);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctl->unit_full[i], 1);
+            mbar_init(&ctl->unit_empty[i], 5);
+        }
+        mbar_init(&ctl->p_full, 256);
         mbar_init(&ctl->o_done, 1);
-        mbar_init(&ctl->o_free, 128);
-        mbar_init(&ctl->drain, 1);
+        mbar_init(&ctl->o_free, 256);
+        mbar_init(&ctl->drain_s, 1);
+        mbar_init(&ctl->drain_pv, 1);
         ctl->abort_flag = 0;
         fence_barrier_init();
         fence_proxy_async_smem();
@@ -195,31 +291,29 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
     const uint32_t tmem = ctl->tmem_base;
     const int n_units = p.ctrl[0];
 
+    // Consumer side of the unit ring (S issuer, V producer, PV issuer): returns false at the
+    // end of the work or on abort.
+    auto next_unit = [&](uint32_t &k, UnitInfo &u) -> bool {
+        const int e = k & 1;
+        if (!mbar_wait(&ctl->unit_full[e], (k >> 1) & 1, abort_flag, p.dev_error, lim)) return false;
+        u = ctl->unit[e];
+        mbar_arrive(&ctl->unit_empty[e]);
+        ++k;
+        return u.valid != 0;
+    };
+    auto tile_rows = [&](const UnitInfo &u, int tile, int &r0, int &r1) {
+        const int pg = 2 * tile;
+        r0 = p.comp_slot[u.comp_base + pg] * 64;
+        r1 = (pg + 1 < u.n_pages) ? p.comp_slot[u.comp_base + pg + 1] * 64 : p.oob_row;
+    };
+
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ---------------------------------------------------------------- K-stream TMA
         if (lane == 0) {
-            prefetch_tmap(&maps.q);
-            uint32_t ring_pos = 0, q_cnt = 0, k = 0;
+            prefetch_tmap(&maps.q[0]);
+            const uint64_t pol = make_policy_evict_last();
+            uint32_t kpos = 0, q_cnt = 0, k = 0;
             bool ok = true;
-            auto load_block = [&](const CUtensorMap *km, int kb, int row0, int row1) -> bool {
-                const uint32_t slot = ring_pos % kRingSlots;
-                const uint32_t par = ((ring_pos / kRingSlots) & 1) ^ 1;
-                ++ring_pos;
-                if (!mbar_wait(&ctl->empty[slot], par, abort_flag, p.dev_error, lim)) return false;
-                mbar_arrive_expect_tx(&ctl->full[slot], kBlockBytes);
-                uint8_t *dst = ring + slot * kBlockBytes;
-                tma_load_2d(dst, km, &ctl->full[slot], kb * 64, row0);
-                tma_load_2d(dst + kHalfBlock, km, &ctl->full[slot], kb * 64, row1);
-                return true;
-            };
-            auto pad_block = [&]() -> bool {
-                const uint32_t slot = ring_pos % kRingSlots;
-                const uint32_t par = ((ring_pos / kRingSlots) & 1) ^ 1;
-                ++ring_pos;
-                if (!mbar_wait(&ctl->empty[slot], par, abort_flag, p.dev_error, lim)) return false;
-                mbar_arrive(&ctl->full[slot]);
-                return true;
-            };
             while (ok) {
                 const int e = k & 1;
                 if (!mbar_wait(&ctl->unit_empty[e], ((k >> 1) & 1) ^ 1, abort_flag, p.dev_error, lim)) {
@@ -249,37 +343,47 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                 if (!u.valid) break;
                 const int nt = (u.n_pages + 1) >> 1;
                 if (nt == 0) continue;
-                const CUtensorMap *km = &maps.kv[u.d];
                 if (!mbar_wait(&ctl->q_empty, (q_cnt & 1) ^ 1, abort_flag, p.dev_error, lim)) {
                     ok = false;
                     break;
                 }
                 ++q_cnt;
                 mbar_arrive_expect_tx(&ctl->q_full, kQBytes);
-                for (int kb = 0; kb < kQBlocks; ++kb)
-                    tma_load_2d(sq + kb * kHalfBlock, &maps.q, &ctl->q_full, kb * 64, u.q_row0);
-                auto rows_of = [&](int tile, int &r0, int &r1) {
-                    const int pg = 2 * tile;
-                    r0 = p.comp_slot[u.comp_base + pg] * 64;
-                    r1 = (pg + 1 < u.n_pages) ? p.comp_slot[u.comp_base + pg + 1] * 64 : p.oob_row;
-                };
-                auto load_S = [&](int tile) -> bool {
+                if (F8) {
+                    for (int b = 0; b < 4; ++b) {
+                        tma_load_2d(sq + b * 16384, &maps.q[0], &ctl->q_full, b * 128, u.q_row0);
+                        tma_load_2d(sq + b * 16384 + 8192, &maps.q[0], &ctl->q_full, b * 128, p.R + u.q_row0);
+                    }
+                    tma_load_2d(sq + 65536, &maps.q[1], &ctl->q_full, 512, u.q_row0);
+                    tma_load_2d(sq + 65536 + 4096, &maps.q[1], &ctl->q_full, 512, p.R + u.q_row0);
+                } else {
+                    for (int kb = 0; kb < 9; ++kb)
+                        tma_load_2d(sq + kb * 8192, &maps.q[0], &ctl->q_full, kb * 64, u.q_row0);
+                }
+                const CUtensorMap *km = maps.kv[u.d];
+                for (int i = 0; i < nt && ok; ++i) {
                     int r0, r1;
-                    rows_of(tile, r0, r1);
-                    for (int kb = 0; kb < kQBlocks; ++kb)
-                        if (!load_block(km, kb, r0, r1)) return false;
-                    return pad_block();
-                };
-                auto load_V = [&](int tile) -> bool {
-                    int r0, r1;
-                    rows_of(tile, r0, r1);
-                    for (int kb = 0; kb < kVBlocks; ++kb)
-                        if (!load_block(km, kb, r0, r1)) return false;
-                    return true;
-                };
-                ok = load_S(0);
-                for (int i = 1; i < nt && ok; ++i) ok = load_S(i) && load_V(i - 1);
-                if (ok) ok = load_V(nt - 1);
+                    tile_rows(u, i, r0, r1);
+                    for (int kb = 0; kb < C::kKBlocks; ++kb) {
+                        const uint32_t slot = kpos % kKSlots;
+                        if (!mbar_wait(&ctl->kempty[slot], ((kpos / kKSlots) & 1) ^ 1, abort_flag, p.dev_error, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        ++kpos;
+                        uint8_t *dst = kring + slot * kKSlotBytes;
+                        if (F8 && kb == 4) {  // rope: 64 dims, 64-byte swizzle, 4 KB per page
+                            mbar_arrive_expect_tx(&ctl->kfull[slot], 8192);
+                            tma_load_2d_hint(dst, &km[1], &ctl->kfull[slot], 512, r0, pol);
+                            tma_load_2d_hint(dst + 4096, &km[1], &ctl->kfull[slot], 512, r1, pol);
+                        } else {
+                            const int x = F8 ? kb * 128 : kb * 64;
+                            mbar_arrive_expect_tx(&ctl->kfull[slot], kKSlotBytes);
+                            tma_load_2d_hint(dst, &km[0], &ctl->kfull[slot], x, r0, pol);
+                            tma_load_2d_hint(dst + 8192, &km[0], &ctl->kfull[slot], x, r1, pol);
+                        }
+                    }
+                }
             }
             if (!ok) {  // let issued TMA copies land before the CTA can exit
                 const uint64_t t0 = global_timer_ns();
@@ -288,114 +392,192 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ---------------------------------------------------------------- score MMAs
         if (lane == 0) {
-            uint32_t ring_pos = 0, s_cnt = 0, p_cnt = 0, q_cnt = 0, of_cnt = 0, k = 0;
-            bool had_tiles = false, ok = true;
-            const uint32_t ring_addr = smem_u32(ring), q_addr = smem_u32(sq), p_addr = smem_u32(sp);
-            auto issue_S = [&]() -> bool {
-                const uint32_t sb = s_cnt & 1;
-                if (!mbar_wait(&ctl->s_free[sb], ((s_cnt >> 1) & 1) ^ 1, abort_flag, p.dev_error, lim)) return false;
-                ++s_cnt;
-                tc_fence_after();
-                const uint32_t d_tmem = tmem + kSCol + 64 * sb;
-                for (int kb = 0; kb < kQBlocks; ++kb) {
-                    const uint32_t slot = ring_pos % kRingSlots;
-                    if (!mbar_wait(&ctl->full[slot], (ring_pos / kRingSlots) & 1, abort_flag, p.dev_error, lim)) return false;
-                    ++ring_pos;
-                    tc_fence_after();
-                    const uint32_t a0 = ring_addr + slot * kBlockBytes;
-                    const uint32_t b0 = q_addr + kb * kHalfBlock;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_f16_ss(d_tmem, smem_desc_sw128(a0 + kk * 32, 16, 1024),
-                                   smem_desc_sw128(b0 + kk * 32, 16, 1024), kIdescS, (kb | kk) != 0);
-                    mma_commit(&ctl->empty[slot]);
-                }
-                {   // pad position of the ring
-                    const uint32_t slot = ring_pos % kRingSlots;
-                    if (!mbar_wait(&ctl->full[slot], (ring_pos / kRingSlots) & 1, abort_flag, p.dev_error, lim)) return false;
-                    ++ring_pos;
-                    mbar_arrive(&ctl->empty[slot]);
-                }
-                mma_commit(&ctl->s_full[sb]);
-                return true;
-            };
-            auto issue_PV = [&](bool first) -> bool {
-                if (!mbar_wait(&ctl->p_full, p_cnt & 1, abort_flag, p.dev_error, lim)) return false;
-                ++p_cnt;
-                if (first && had_tiles) {
-                    if (!mbar_wait(&ctl->o_free, of_cnt & 1, abort_flag, p.dev_error, lim)) return false;
-                    ++of_cnt;
-                }
-                tc_fence_after();
-                for (int j = 0; j < kVBlocks / 2; ++j) {
-                    const uint32_t sa = ring_pos % kRingSlots;
-                    if (!mbar_wait(&ctl->full[sa], (ring_pos / kRingSlots) & 1, abort_flag, p.dev_error, lim)) return false;
-                    ++ring_pos;
-                    const uint32_t sb2 = ring_pos % kRingSlots;
-                    if (!mbar_wait(&ctl->full[sb2], (ring_pos / kRingSlots) & 1, abort_flag, p.dev_error, lim)) return false;
-                    ++ring_pos;
-                    tc_fence_after();
-                    const uint32_t a0 = ring_addr + sa * kBlockBytes;
-                    const uint32_t d_tmem = tmem + 64 * j;
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_f16_ss(d_tmem, smem_desc_sw128(a0 + kk * 2048, kBlockBytes, 1024),
-                                   smem_desc_sw128(p_addr + kk * 2048, 1024, 1024), kIdescPV,
-                                   !(first && kk == 0));
-                    mma_commit(&ctl->empty[sa]);
-                    mma_commit(&ctl->empty[sb2]);
-                }
-                mma_commit(&ctl->o_done);
-                return true;
-            };
-            while (ok) {
-                const int e = k & 1;
-                if (!mbar_wait(&ctl->unit_full[e], (k >> 1) & 1, abort_flag, p.dev_error, lim)) {
-                    ok = false;
-                    break;
-                }
-                const UnitInfo u = ctl->unit[e];
-                mbar_arrive(&ctl->unit_empty[e]);
-                ++k;
-                if (!u.valid) break;
+            uint32_t kpos = 0, s_cnt = 0, q_cnt = 0, k = 0;
+            bool ok = true;
+            const uint32_t kaddr = smem_u32(kring), q_addr = smem_u32(sq);
+            UnitInfo u;
+            while (ok && next_unit(k, u)) {
                 const int nt = (u.n_pages + 1) >> 1;
                 if (nt == 0) continue;
-                if (!mbar_wait(&ctl->q_full, q_cnt & 1, abort_flag, p.dev_error, lim)) {
-                    ok = false;
-                    break;
-                }
+                if (!mbar_wait(&ctl->q_full, q_cnt & 1, abort_flag, p.dev_error, lim)) break;
                 ++q_cnt;
                 tc_fence_after();
                 for (int i = 0; i < nt && ok; ++i) {
-                    ok = issue_S();
-                    if (ok && i == nt - 1) mma_commit(&ctl->q_empty);
-                    if (ok && i > 0) ok = issue_PV(i - 1 == 0);
+                    const uint32_t sb = s_cnt % C::kSBufs;
+                    if (!mbar_wait(&ctl->s_free[sb], ((s_cnt / C::kSBufs) & 1) ^ 1, abort_flag, p.dev_error, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    ++s_cnt;
+                    tc_fence_after();
+                    const uint32_t d_tmem = tmem + kSCol + C::kSCols * sb;
+                    for (int kb = 0; kb < C::kKBlocks; ++kb) {
+                        const uint32_t slot = kpos % kKSlots;
+                        if (!mbar_wait(&ctl->kfull[slot], (kpos / kKSlots) & 1, abort_flag, p.dev_error, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        ++kpos;
+                        tc_fence_after();
+                        const uint32_t a0 = kaddr + slot * kKSlotBytes;
+                        if (F8) {
+                            if (kb < 4) {
+                                const uint32_t b0 = q_addr + kb * 16384;
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk)
+                                    mma_f8_ss(d_tmem, smem_desc(a0 + kk * 32, 16, 1024, kSwizzle128),
+                                              smem_desc(b0 + kk * 32, 16, 1024, kSwizzle128), C::kIdescS,
+                                              (kb | kk) != 0);
+                            } else {
+                                const uint32_t b0 = q_addr + 65536;
+#pragma unroll
+                                for (int kk = 0; kk < 2; ++kk)
+                                    mma_f8_ss(d_tmem, smem_desc(a0 + kk * 32, 16, 512, kSwizzle64),
+                                              smem_desc(b0 + kk * 32, 16, 512, kSwizzle64), C::kIdescS, 1);
+                            }
+                        } else {
+                            const uint32_t b0 = q_addr + kb * 8192;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_f16_ss(d_tmem, smem_desc(a0 + kk * 32, 16, 1024, kSwizzle128),
+                                           smem_desc(b0 + kk * 32, 16, 1024, kSwizzle128), C::kIdescS,
+                                           (kb | kk) != 0);
+                        }
+                        mma_commit(&ctl->kempty[slot]);
+                    }
+                    if (!ok) break;
+                    mma_commit(&ctl->s_full[sb]);
+                    if (i == nt - 1) mma_commit(&ctl->q_empty);
                 }
-                if (ok) ok = issue_PV(nt == 1);
+            }
+            mma_commit(&ctl->drain_s);
+            int never = 0;
+            mbar_wait(&ctl->drain_s, 0, &never, nullptr, 100000000ull);
+        }
+    } else if (warp == 2) {
+        // ---------------------------------------------------------------- V-stream TMA
+        if (lane == 0) {
+            const uint64_t pol = make_policy_evict_first();
+            uint32_t vpos = 0, k = 0;
+            bool ok = true;
+            UnitInfo u;
+            while (ok && next_unit(k, u)) {
+                const int nt = (u.n_pages + 1) >> 1;
+                const CUtensorMap *km = &maps.kv[u.d][0];
+                for (int i = 0; i < nt && ok; ++i) {
+                    int r0, r1;
+                    tile_rows(u, i, r0, r1);
+                    for (int vu = 0; vu < C::kVUnits; ++vu) {
+                        const uint32_t slot = vpos % kVSlots;
+                        if (!mbar_wait(&ctl->vempty[slot], ((vpos / kVSlots) & 1) ^ 1, abort_flag, p.dev_error, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        ++vpos;
+                        uint8_t *dst = vring + slot * kVSlotBytes;
+                        mbar_arrive_expect_tx(&ctl->vfull[slot], kVSlotBytes);
+                        const int w = F8 ? 128 : 64;  // dims per block
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int x = (2 * vu + h) * w;
+                            tma_load_2d_hint(dst + h * 16384, km, &ctl->vfull[slot], x, r0, pol);
+                            tma_load_2d_hint(dst + h * 16384 + 8192, km, &ctl->vfull[slot], x, r1, pol);
+                        }
+                    }
+                }
+            }
+            if (!ok) {
+                const uint64_t t0 = global_timer_ns();
+                while (global_timer_ns() - t0 < 200000ull) {
+                }
+            }
+        }
+    } else if (warp == 3) {
+        // ---------------------------------------------------------------- P*V MMAs
+        if (lane == 0) {
+            uint32_t vpos = 0, p_cnt = 0, of_cnt = 0, k = 0;
+            bool had_tiles = false, ok = true;
+            const uint32_t vaddr = smem_u32(vring), p_addr = smem_u32(sp);
+            UnitInfo u;
+            while (ok && next_unit(k, u)) {
+                const int nt = (u.n_pages + 1) >> 1;
+                if (nt == 0) continue;
+                for (int i = 0; i < nt && ok; ++i) {
+                    if (!mbar_wait(&ctl->p_full, p_cnt & 1, abort_flag, p.dev_error, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    ++p_cnt;
+                    if (i == 0 && had_tiles) {
+                        if (!mbar_wait(&ctl->o_free, of_cnt & 1, abort_flag, p.dev_error, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        ++of_cnt;
+                    }
+                    tc_fence_after();
+                    for (int vu = 0; vu < C::kVUnits; ++vu) {
+                        const uint32_t slot = vpos % kVSlots;
+                        if (!mbar_wait(&ctl->vfull[slot], (vpos / kVSlots) & 1, abort_flag, p.dev_error, lim)) {
+                            ok = false;
+                            break;
+                        }
+                        ++vpos;
+                        tc_fence_after();
+                        const uint32_t a0 = vaddr + slot * kVSlotBytes;
+                        if (F8) {
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {  // two 128-dim blocks = two M-tiles
+                                const uint32_t d_tmem = tmem + 64 * (2 * vu + h);
+#pragma unroll
+                                for (int kk = 0; kk < 4; ++kk) {
+                                    const uint64_t ad = smem_desc(a0 + h * 16384 + kk * 4096, 16384, 1024, kSwizzle128);
+                                    mma_f8_ss(d_tmem, ad, smem_desc(p_addr + kk * 2048, 512, 512, kSwizzle64),
+                                              C::kIdescPV, !(i == 0 && kk == 0));
+                                    mma_f8_ss(d_tmem, ad, smem_desc(p_addr + 8192 + kk * 2048, 512, 512, kSwizzle64),
+                                              C::kIdescPV, 1);
+                                }
+                            }
+                        } else {
+                            const uint32_t d_tmem = tmem + 64 * vu;
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk)
+                                mma_f16_ss(d_tmem, smem_desc(a0 + kk * 2048, 16384, 1024, kSwizzle128),
+                                           smem_desc(p_addr + kk * 2048, 1024, 1024, kSwizzle128), C::kIdescPV,
+                                           !(i == 0 && kk == 0));
+                        }
+                        mma_commit(&ctl->vempty[slot]);
+                    }
+                    if (!ok) break;
+                    mma_commit(&ctl->o_done);
+                }
                 had_tiles = true;
             }
-            // drain: every MMA issued so far has completed once `drain` flips
-            mma_commit(&ctl->drain);
+            mma_commit(&ctl->drain_pv);
             int never = 0;
-            mbar_wait(&ctl->drain, 0, &never, nullptr, 100000000ull);
+            mbar_wait(&ctl->drain_pv, 0, &never, nullptr, 100000000ull);
         }
     } else {
-        // ------------------------------------------------------------ softmax warps
-        const int stid = threadIdx.x - 64;          // 0..127
+        // ---------------------------------------------------------------- softmax warps
+        // Two independent warpgroups; warpgroup g owns query columns [32g, 32g + 32) of every
+        // tile.  Within a warpgroup each thread owns one token row (TMEM lane).
+        const int wg = (warp - 4) >> 2;             // 0 or 1
+        const int gtid = threadIdx.x - 128 - 128 * wg;  // 0..127 within the warpgroup
         const int quad = warp & 3;                  // TMEM lane quadrant of this warp
         const int row = quad * 32 + lane;           // token row of the tile = TMEM lane
-        const int wl = warp - 2;                    // 0..3 for the reduction scratch
+        const int c0 = 32 * wg;                     // first query column of this warpgroup
+        const int bar_a = 1 + 2 * wg, bar_b = 2 + 2 * wg;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
         uint32_t s_cnt = 0, od_cnt = 0, k = 0;
         while (true) {
             const int e = k & 1;
             int fail = !warp_wait(&ctl->unit_full[e], (k >> 1) & 1, abort_flag, p.dev_error, lim);
-            if (named_bar_or(1, 128, fail)) break;
+            if (named_bar_or(bar_a, 128, fail)) break;
             const UnitInfo u = ctl->unit[e];
-            named_bar_sync(2, 128);
-            if (stid == 0) mbar_arrive(&ctl->unit_empty[e]);
+            named_bar_sync(bar_b, 128);
+            if (gtid == 0) mbar_arrive(&ctl->unit_empty[e]);
             ++k;
             if (!u.valid) break;
             const int nt = (u.n_pages + 1) >> 1;
@@ -406,111 +588,154 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
             float *obase = direct ? p.o_part : p.part_o;
             float *lbase = direct ? p.lse_part : p.part_lse;
             if (nt == 0) {
-                for (int idx = stid; idx < u.rows_valid * (kVDim / 4); idx += 128) {
-                    const int c = idx / (kVDim / 4), v4 = idx - c * (kVDim / 4);
-                    reinterpret_cast<float4 *>(obase + (out_row0 + c) * kVDim)[v4] = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int idx = gtid; idx < 32 * (kVDim / 4); idx += 128) {
+                    const int c = c0 + idx / (kVDim / 4), v4 = idx % (kVDim / 4);
+                    if (c < u.rows_valid)
+                        reinterpret_cast<float4 *>(obase + (out_row0 + c) * kVDim)[v4] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                if (stid < u.rows_valid) lbase[out_row0 + stid] = -INFINITY;
+                if (gtid < 32 && c0 + gtid < u.rows_valid) lbase[out_row0 + c0 + gtid] = -INFINITY;
                 continue;
             }
-            if (stid < 64) ctl->m_run[stid] = -INFINITY;
-            float lp[64];
+            if (gtid < 32) {
+                ctl->m_run[c0 + gtid] = -INFINITY;
+                float qs = p.sl2;
+                if (F8) {
+                    const int qr = u.q_row0 + c0 + gtid;
+                    qs *= (qr < p.R) ? p.q_rscale[qr] : 0.f;
+                }
+                ctl->qscale[c0 + gtid] = qs;
+            }
+            named_bar_sync(bar_b, 128);
+            float lp[32];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) lp[c] = 0.f;
+            for (int c = 0; c < 32; ++c) lp[c] = 0.f;
+            // page index of this row's page in tile 0, then prefetched one tile ahead
+            int j_cur = -1;
+            {
+                const int pl = row >> 6;
+                if (pl < u.n_pages) j_cur = p.comp_page[u.comp_base + pl];
+            }
             bool aborted = false;
             for (int i = 0; i < nt; ++i) {
-                const uint32_t sb = s_cnt & 1;
-                fail = !warp_wait(&ctl->s_full[sb], (s_cnt >> 1) & 1, abort_flag, p.dev_error, lim);
+                int j_next = -1;
+                {
+                    const int pl = 2 * (i + 1) + (row >> 6);
+                    if (i + 1 < nt && pl < u.n_pages) j_next = p.comp_page[u.comp_base + pl];
+                }
+                const uint32_t sb = s_cnt % C::kSBufs;
+                fail = !warp_wait(&ctl->s_full[sb], (s_cnt / C::kSBufs) & 1, abort_flag, p.dev_error, lim);
                 ++s_cnt;
-                float s[64];
+                float s[32];
                 if (!fail) {
                     tc_fence_after();
-                    {
+                    const uint32_t ta = tmem + lane_base + kSCol + C::kSCols * sb + c0;
+                    tmem_ld32(ta, s);
+                    if (F8) {
                         float t32[32];
-                        tmem_ld32(tmem + lane_base + kSCol + 64 * sb, t32);
+                        tmem_ld32(ta + 64, t32);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) s[c] = t32[c];
-                        tmem_ld32(tmem + lane_base + kSCol + 64 * sb + 32, t32);
+                        for (int c = 0; c < 32; ++c) s[c] += t32[c];
+                    } else {
                         tmem_wait_ld();
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) s[32 + c] = t32[c];
                     }
                     tc_fence_before();
                     mbar_arrive(&ctl->s_free[sb]);
                     // mask: ragged last page / missing second page / causal limit
-                    const int pl = 2 * i + (row >> 6);
-                    bool valid = pl < u.n_pages;
-                    if (valid) {
-                        const int j = p.comp_page[u.comp_base + pl];
-                        valid = (long long)j * 64 + (row & 63) <= (long long)u.limit;
-                    }
+                    const bool valid = j_cur >= 0 && (long long)j_cur * 64 + (row & 63) <= (long long)u.limit;
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) s[c] = valid ? s[c] * p.sl2 : -INFINITY;
-                    float r[32];
-                    reduce_scatter64<true>(s, r, lane);
-                    *reinterpret_cast<float2 *>(&ctl->red[wl][2 * lane]) = make_float2(r[0], r[1]);
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 q4 = *reinterpret_cast<const float4 *>(&ctl->qscale[c0 + c]);
+                        s[c] = valid ? s[c] * q4.x : -INFINITY;
+                        s[c + 1] = valid ? s[c + 1] * q4.y : -INFINITY;
+                        s[c + 2] = valid ? s[c + 2] * q4.z : -INFINITY;
+                        s[c + 3] = valid ? s[c + 3] * q4.w : -INFINITY;
+                    }
+                    const float r = reduce_scatter32<true>(s, lane);
+                    ctl->red[wg][quad][lane] = r;
                 }
-                if (named_bar_or(1, 128, fail)) {
+                j_cur = j_next;
+                if (named_bar_or(bar_a, 128, fail)) {
                     aborted = true;
                     break;
                 }
                 int changed = 0;
-                if (stid < 64) {
-                    const float mt = fmaxf(fmaxf(ctl->red[0][stid], ctl->red[1][stid]),
-                                           fmaxf(ctl->red[2][stid], ctl->red[3][stid]));
-                    const float mo = ctl->m_run[stid];
+                if (gtid < 32) {
+                    const int c = c0 + gtid;
+                    const float mt = fmaxf(fmaxf(ctl->red[wg][0][gtid], ctl->red[wg][1][gtid]),
+                                           fmaxf(ctl->red[wg][2][gtid], ctl->red[wg][3][gtid]));
+                    const float mo = ctl->m_run[c];
                     const float mn = fmaxf(mo, mt);
-                    const float cr = (mn == mo) ? 1.f : exp2f(mo - mn);
-                    ctl->m_run[stid] = mn;
-                    ctl->corr[stid] = cr;
+                    const float cr = (mn == mo) ? 1.f : fast_exp2(mo - mn);
+                    ctl->m_run[c] = mn;
+                    ctl->corr[c] = cr;
                     changed = cr != 1.f;
                 }
-                const int any = named_bar_or(2, 128, changed);
+                const int any = named_bar_or(bar_b, 128, changed);
 #pragma unroll
-                for (int c = 0; c < 64; c += 4) {
-                    const float4 m4 = *reinterpret_cast<const float4 *>(&ctl->m_run[c]);
+                for (int c = 0; c < 32; c += 4) {
+                    const float4 m4 = *reinterpret_cast<const float4 *>(&ctl->m_run[c0 + c]);
                     float4 c4 = make_float4(1.f, 1.f, 1.f, 1.f);
-                    if (any) c4 = *reinterpret_cast<const float4 *>(&ctl->corr[c]);
+                    if (any) c4 = *reinterpret_cast<const float4 *>(&ctl->corr[c0 + c]);
                     const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
                     const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const float ms = mm[q] == -INFINITY ? 0.f : mm[q];
-                        s[c + q] = exp2f(s[c + q] - ms);
+                        s[c + q] = fast_exp2(s[c + q] - ms);
                         lp[c + q] = fmaf(lp[c + q], cc[q], s[c + q]);
                     }
                 }
                 if (i > 0) {
                     fail = !warp_wait(&ctl->o_done, od_cnt & 1, abort_flag, p.dev_error, lim);
                     ++od_cnt;
-                    if (fail) continue;  // the next OR-barrier takes every thread out
+                    if (fail) continue;  // the next OR-barrier takes the warpgroup out
                     tc_fence_after();
                     if (any) {
 #pragma unroll 1
-                        for (int j = 0; j < 8; ++j) {
+                        for (int j = 0; j < 4; ++j) {
                             float o32[32];
-                            const uint32_t ta = tmem + lane_base + 32 * j;
+                            const uint32_t ta = tmem + lane_base + 64 * j + c0;
                             tmem_ld32(ta, o32);
                             tmem_wait_ld();
-                            const float *cr = &ctl->corr[(j & 1) * 32];
 #pragma unroll
-                            for (int c = 0; c < 32; ++c) o32[c] *= cr[c];
+                            for (int c = 0; c < 32; ++c) o32[c] *= ctl->corr[c0 + c];
                             tmem_st32(ta, o32);
                         }
                         tmem_wait_st();
                     }
                 }
-                // P^T row `row`: 64 BF16 values, MN-major with the 128-byte swizzle
-                uint8_t *prow = sp + (row >> 3) * 1024 + (row & 7) * 128;
+                if (F8) {
+                    // P^T row as hi and lo E4M3 rows of 64 bytes, MN-major, 64-byte swizzle;
+                    // this warpgroup writes 16-byte chunks 2wg and 2wg + 1 of each.
+                    const uint32_t off = (row >> 3) * 512 + (row & 7) * 64;
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    uint4 w;
-                    w.x = pack_bf16(s[8 * cc + 0], s[8 * cc + 1]);
-                    w.y = pack_bf16(s[8 * cc + 2], s[8 * cc + 3]);
-                    w.z = pack_bf16(s[8 * cc + 4], s[8 * cc + 5]);
-                    w.w = pack_bf16(s[8 * cc + 6], s[8 * cc + 7]);
-                    *reinterpret_cast<uint4 *>(prow + ((cc ^ (row & 7)) << 4)) = w;
+                    for (int h = 0; h < 2; ++h) {
+                        uint4 hv, lv;
+                        const float *v = s + 16 * h;
+                        split_e4m3x4(v[0] * kPScale, v[1] * kPScale, v[2] * kPScale, v[3] * kPScale, hv.x, lv.x);
+                        split_e4m3x4(v[4] * kPScale, v[5] * kPScale, v[6] * kPScale, v[7] * kPScale, hv.y, lv.y);
+                        split_e4m3x4(v[8] * kPScale, v[9] * kPScale, v[10] * kPScale, v[11] * kPScale, hv.z, lv.z);
+                        split_e4m3x4(v[12] * kPScale, v[13] * kPScale, v[14] * kPScale, v[15] * kPScale, hv.w, lv.w);
+                        const int cc = 2 * wg + h;
+                        const uint32_t sw = ((cc ^ ((row >> 1) & 3)) << 4);
+                        *reinterpret_cast<uint4 *>(sp + off + sw) = hv;
+                        *reinterpret_cast<uint4 *>(sp + 8192 + off + sw) = lv;
+                    }
+                } else {
+                    // P^T row: 64 BF16 values, MN-major with the 128-byte swizzle; this
+                    // warpgroup writes 16-byte chunks 4wg .. 4wg + 3.
+                    uint8_t *prow = sp + (row >> 3) * 1024 + (row & 7) * 128;
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        uint4 w;
+                        w.x = pack_bf16(s[8 * h + 0], s[8 * h + 1]);
+                        w.y = pack_bf16(s[8 * h + 2], s[8 * h + 3]);
+                        w.z = pack_bf16(s[8 * h + 4], s[8 * h + 5]);
+                        w.w = pack_bf16(s[8 * h + 6], s[8 * h + 7]);
+                        const int cc = 4 * wg + h;
+                        *reinterpret_cast<uint4 *>(prow + ((cc ^ (row & 7)) << 4)) = w;
+                    }
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -520,28 +745,25 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
             fail = !warp_wait(&ctl->o_done, od_cnt & 1, abort_flag, p.dev_error, lim);
             ++od_cnt;
             tc_fence_after();
-            {
-                float r[32];
-                reduce_scatter64<false>(lp, r, lane);
-                *reinterpret_cast<float2 *>(&ctl->red[wl][2 * lane]) = make_float2(r[0], r[1]);
-            }
-            if (named_bar_or(1, 128, fail)) break;
-            if (stid < 64) {
-                const float L = ctl->red[0][stid] + ctl->red[1][stid] + ctl->red[2][stid] + ctl->red[3][stid];
-                const float mr = ctl->m_run[stid];
+            ctl->red[wg][quad][lane] = reduce_scatter32<false>(lp, lane);
+            if (named_bar_or(bar_a, 128, fail)) break;
+            if (gtid < 32) {
+                const int c = c0 + gtid;
+                const float L = ctl->red[wg][0][gtid] + ctl->red[wg][1][gtid] + ctl->red[wg][2][gtid] +
+                                ctl->red[wg][3][gtid];
+                const float mr = ctl->m_run[c];
                 const bool live = L > 0.f;
-                ctl->oscale[stid] = live ? p.kv_scale / L : 0.f;
-                if (stid < u.rows_valid)
-                    lbase[out_row0 + stid] = live ? (mr + log2f(L)) * 0.69314718055994531f : -INFINITY;
+                ctl->oscale[c] = live ? p.out_scale / L : 0.f;
+                if (c < u.rows_valid)
+                    lbase[out_row0 + c] = live ? (mr + log2f(L)) * 0.69314718055994531f : -INFINITY;
             }
-            named_bar_sync(2, 128);
+            named_bar_sync(bar_b, 128);
 #pragma unroll 1
-            for (int j = 0; j < 8; ++j) {
+            for (int j = 0; j < 4; ++j) {
                 float o32[32];
-                tmem_ld32(tmem + lane_base + 32 * j, o32);
+                tmem_ld32(tmem + lane_base + 64 * j + c0, o32);
                 tmem_wait_ld();
-                const int vcol = (j >> 1) * 128 + row;  // V dimension held by this lane
-                const int c0 = (j & 1) * 32;
+                const int vcol = j * 128 + row;  // V dimension held by this lane
 #pragma unroll
                 for (int c = 0; c < 32; ++c)
                     if (c0 + c < u.rows_valid)
@@ -740,16 +962,18 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// 2-D BF16 map over [rows][576] with 64 x 64 boxes and the 128-byte swizzle.
-bool make_map_bf16(CUtensorMap *m, const void *ptr, uint64_t rows) {
+// 2-D map over [rows][576] elements (BF16 or bytes) with a box of box_x elements by 64 rows.
+bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, bool bf16, uint32_t box_x, bool swz128) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
+    const uint32_t esz = bf16 ? 2 : 1;
     cuuint64_t dims[2] = {(cuuint64_t)kKDim, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)kKDim * 2};
-    cuuint32_t box[2] = {64, 64};
+    cuuint64_t strides[1] = {(cuuint64_t)kKDim * esz};
+    cuuint32_t box[2] = {box_x, 64};
     cuuint32_t estr[2] = {1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    return enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr),
+               dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               swz128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -801,13 +1025,25 @@ bool plan_attention(int B, int T, int H, int N, int64_t num_pages, int dtype, in
     s->off_ctrl = off;    off = align256(off + sizeof(int32_t) * 4);
     s->off_part_o = off;  off = align256(off + sizeof(float) * (size_t)s->max_partials * kGroupRows * kVDim);
     s->off_part_lse = off; off = align256(off + sizeof(float) * (size_t)s->max_partials * kGroupRows);
+    const size_t R = (size_t)B * T * H;
+    s->off_qhl = off;     off = align256(off + (dtype == DCP_KV_FP8_E4M3 ? 2 * R * kKDim : 0));
+    s->off_qscale = off;  off = align256(off + (dtype == DCP_KV_FP8_E4M3 ? sizeof(float) * R : 0));
     s->total_bytes = off;
     return true;
 }
 
+template <bool F8>
+int launch_kernel(const AttnMaps &maps, const KParams &kp, int grid, cudaStream_t stream) {
+    if (cudaFuncSetAttribute(attn_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+        cudaSuccess)
+        return DCP_ERR_CUDA;
+    attn_kernel<F8><<<grid, kThreads, kSmemBytes, stream>>>(maps, kp);
+    return cudaGetLastError() == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
 int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     const AttnPlanShape &s = a.shape;
-    if (a.dtype != DCP_KV_BF16) return DCP_ERR_UNSUPPORTED;
+    const bool f8 = a.dtype == DCP_KV_FP8_E4M3;
     if (s.B == 0) return DCP_OK;
     uint8_t *ws = a.workspace;
     int32_t *counts = reinterpret_cast<int32_t *>(ws + s.off_counts);
@@ -819,6 +1055,9 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     int *ctrl = reinterpret_cast<int *>(ws + s.off_ctrl);
     float *part_o = reinterpret_cast<float *>(ws + s.off_part_o);
     float *part_lse = reinterpret_cast<float *>(ws + s.off_part_lse);
+    uint8_t *qhl = ws + s.off_qhl;
+    float *qscale = reinterpret_cast<float *>(ws + s.off_qscale);
+    const int R = s.B * s.T * s.H;
 
     const int warps_per_block = 4;
     plan_pages_kernel<<<(s.B + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, stream>>>(
@@ -828,12 +1067,26 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     plan_units_kernel<<<1, kPlanThreads, 0, stream>>>(s.B, s.N, s.G, a.only_rank, s.tiles_per_chunk, counts,
                                                        pair_chunks, pair_part, units, ctrl);
     if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
+    if (f8) {
+        q_split_kernel<<<(R + 7) / 8, 256, 0, stream>>>(R, reinterpret_cast<const __nv_bfloat16 *>(a.q), qhl, qscale);
+        if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
+    }
 
     AttnMaps maps;
     memset(&maps, 0, sizeof(maps));
-    if (!make_map_bf16(&maps.q, a.q, (uint64_t)s.B * s.T * s.H)) return DCP_ERR_CUDA;
-    for (int d = 0; d < s.N; ++d)
-        if (!make_map_bf16(&maps.kv[d], a.kv_pools[d], (uint64_t)a.slots_per_rank * kPage)) return DCP_ERR_CUDA;
+    const uint64_t pool_rows = (uint64_t)a.slots_per_rank * kPage;
+    if (f8) {
+        if (!make_map(&maps.q[0], qhl, 2ull * R, false, 128, true) || !make_map(&maps.q[1], qhl, 2ull * R, false, 64, false))
+            return DCP_ERR_CUDA;
+        for (int d = 0; d < s.N; ++d)
+            if (!make_map(&maps.kv[d][0], a.kv_pools[d], pool_rows, false, 128, true) ||
+                !make_map(&maps.kv[d][1], a.kv_pools[d], pool_rows, false, 64, false))
+                return DCP_ERR_CUDA;
+    } else {
+        if (!make_map(&maps.q[0], a.q, (uint64_t)R, true, 64, true)) return DCP_ERR_CUDA;
+        for (int d = 0; d < s.N; ++d)
+            if (!make_map(&maps.kv[d][0], a.kv_pools[d], pool_rows, true, 64, true)) return DCP_ERR_CUDA;
+    }
     KParams kp;
     kp.seq_lens = a.seq_lens;
     kp.req_page_ptr = a.req_page_ptr;
@@ -842,28 +1095,27 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     kp.units = units;
     kp.ctrl = ctrl;
     kp.counter = ctrl + 1;
+    kp.q_rscale = qscale;
     kp.B = s.B;
     kp.T = s.T;
     kp.H = s.H;
     kp.HB = (s.H + kGroupRows - 1) / kGroupRows;
     kp.G = s.G;
+    kp.R = R;
     kp.num_pages = s.num_pages;
-    kp.oob_row = (int)std::min<int64_t>((int64_t)a.slots_per_rank * kPage, 0x7fffff00);
-    const float kappa = a.dtype == DCP_KV_FP8_E4M3 ? a.kv_scale : 1.f;
+    kp.oob_row = (int)std::min<int64_t>((int64_t)pool_rows, 0x7fffff00);
+    const float kappa = f8 ? a.kv_scale : 1.f;
     kp.sl2 = a.softmax_scale * kappa * 1.4426950408889634f;
-    kp.kv_scale = kappa;
+    kp.out_scale = f8 ? kappa / kPScale : kappa;
     kp.o_part = a.o_part;
     kp.lse_part = a.lse_part;
     kp.part_o = part_o;
     kp.part_lse = part_lse;
     kp.dev_error = a.dev_error;
     kp.wait_limit_ns = a.wait_limit_ns;
-    if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) != cudaSuccess)
-        return DCP_ERR_CUDA;
-    const long long max_units = s.max_units;
-    const int grid = (int)std::max<long long>(1, std::min<long long>(num_sms, max_units));
-    attn_kernel<<<grid, kThreads, kSmemBytes, stream>>>(maps, kp);
-    if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
+    const int grid = (int)std::max<long long>(1, std::min<long long>(num_sms, s.max_units));
+    const int st = f8 ? launch_kernel<true>(maps, kp, grid, stream) : launch_kernel<false>(maps, kp, grid, stream);
+    if (st != DCP_OK) return st;
     const long long n_tasks = (long long)s.N * s.B * s.G * kGroupRows;
     const int cw = 8;
     combine_kernel<<<(unsigned)((n_tasks + cw - 1) / cw), 32 * cw, 0, stream>>>(

@@ -91,6 +91,28 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, ui
         : "memory");
 }
 
+// Same with an L2 eviction-priority policy (from make_policy_*).
+__device__ __forceinline__ void tma_load_2d_hint(void *smem_dst, const void *tmap, uint64_t *bar,
+                                                 int32_t c0, int32_t c1, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t make_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t make_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
@@ -160,6 +182,17 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, kind::f8f6f4 (8-bit inputs, FP32 accumulate).
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 op this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
     asm volatile(
@@ -214,16 +247,25 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // Shared-memory matrix descriptor (tcgen05): start, leading / stride byte offsets (all >> 4),
-// descriptor version 1 at bits 46-47, layout type at bits 61-63 (2 = 128-byte swizzle).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes) {
+// descriptor version 1 at bits 46-47, layout type at bits 61-63 (2 = 128-byte swizzle,
+// 4 = 64-byte swizzle).
+constexpr uint32_t kSwizzle128 = 2;
+constexpr uint32_t kSwizzle64 = 4;
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t layout) {
     uint64_t d = 0;
     d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
     d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
     d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1 << 46;
-    d |= (uint64_t)2 << 61;
+    d |= (uint64_t)layout << 61;
     return d;
+}
+
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
+                                                    uint32_t sbo_bytes) {
+    return smem_desc(saddr, lbo_bytes, sbo_bytes, kSwizzle128);
 }
 
 // Instruction descriptor, kind::f16: FP32 accumulate, BF16 A and B, given majorness
@@ -236,6 +278,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, int a_mn_maj
            | ((uint32_t)b_mn_major << 16)    // B major
            | ((uint32_t)(n >> 3) << 17)      // N / 8
            | ((uint32_t)(m >> 4) << 24);     // M / 16
+}
+
+// Instruction descriptor, kind::f8f6f4 with E4M3 A and B, FP32 accumulate.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n, int a_mn_major, int b_mn_major) {
+    return (1u << 4)                         // D format FP32
+           | (0u << 7)                       // A format E4M3
+           | (0u << 10)                      // B format E4M3
+           | ((uint32_t)a_mn_major << 15)
+           | ((uint32_t)b_mn_major << 16)
+           | ((uint32_t)(n >> 3) << 17)
+           | ((uint32_t)(m >> 4) << 24);
 }
 
 // ------------------------------------------------------------------------ named barriers

@@ -146,6 +146,11 @@ ATTN_CASES = [
     ("causal-q4", [64 * 7 + 3, 66, 260], 64, 4, 2, "bf16"),
     ("heads-96", [700, 333], 96, 1, 3, "bf16"),
     ("dcp1", [1500], 64, 1, 1, "bf16"),
+    ("tiny-fp8", [1024], 16, 1, 4, "e4m3"),
+    ("ragged-fp8", [1000, 130, 64 * 9 + 5], 64, 1, 4, "e4m3"),
+    ("empty-ranks-fp8", [64, 200, 1], 64, 1, 8, "e4m3"),
+    ("causal-q4-fp8", [64 * 7 + 3, 66, 260], 64, 4, 2, "e4m3"),
+    ("heads-96-fp8", [700, 333], 96, 1, 3, "e4m3"),
 ]
 
 
@@ -156,9 +161,10 @@ def test_attention_matches_oracle(cuda_device, name, lens, H, T, N, dtype):
     _check_all(case, *_run_attention(case))
 
 
-def test_attention_multi_chunk_combine(cuda_device):
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_attention_multi_chunk_combine(cuda_device, dtype):
     """A long single request splits into many chunks per rank (in-call chunk merge)."""
-    case = di.attention_case([64 * 1024 + 17], H=64, T=1, n_dcp=2, dtype="bf16", slots_per_rank=None,
+    case = di.attention_case([64 * 1024 + 17], H=64, T=1, n_dcp=2, dtype=dtype, slots_per_rank=None,
                              seed=21, device=cuda_device, name="long-chunked")
     o, l, om, lm = _run_attention(case)
     rows = np.arange(0, 64, 7)
@@ -182,3 +188,45 @@ def test_attention_batch_full_size_sampled(cuda_device):
         compare(o[d].reshape(-1, 512)[rows], l[d].reshape(-1)[rows], ro, rl, f"batch rank {d}")
     ro, rl = oracle_attention(case, rows=rows, qb=qb, pools=pools)
     compare(om.reshape(-1, 512)[rows], lm.reshape(-1)[rows], ro, rl, "batch merged")
+
+
+def _sampled(case, o, l, om, lm, n_rows, ranks, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = np.sort(rng.choice(case.rows, n_rows, replace=False))
+    qb, pools = q_bits(case), pool_bytes(case)
+    for d in ranks:
+        ro, rl = oracle_attention(case, rank=d, rows=rows, qb=qb, pools=pools)
+        compare(o[d].reshape(-1, 512)[rows], l[d].reshape(-1)[rows], ro, rl, f"{case.name} rank {d}")
+    ro, rl = oracle_attention(case, rows=rows, qb=qb, pools=pools)
+    compare(om.reshape(-1, 512)[rows], lm.reshape(-1)[rows], ro, rl, f"{case.name} merged")
+
+
+def test_attention_agent_full_size_sampled(cuda_device):
+    """48 x 100,000 tokens, 64 heads, FP8-E4M3, DCP=8 over a ~2.8 GB pool; sampled rows."""
+    case = di.agent_case(cuda_device)
+    _sampled(case, *_run_attention(case), n_rows=24, ranks=(0, 7))
+
+
+def test_attention_agent_dcp1_check(cuda_device):
+    """The 1/8 check of the agent workload: 6 requests run at DCP=1 over one pool holding all
+    their pages equal their DCP=8 partials merged."""
+    case = di.agent_case(cuda_device)
+    sub = di.AttnCase(B=6, T=1, H=64, n_dcp=8, dtype="e4m3", seq_lens=case.seq_lens[:6],
+                      req_page_ptr=case.req_page_ptr[:7].clone(),
+                      dst_vpages=case.dst_vpages[:int(case.req_page_ptr[6])].clone(), q=case.q[:6].contiguous(),
+                      pools=case.pools, slots_per_rank=case.slots_per_rank, kv_scale=case.kv_scale, name="agent-6")
+    o8, l8, om, lm = _run_attention(sub)
+    one = torch.cat(sub.pools, 0)
+    vp = (sub.dst_vpages % 8) * sub.slots_per_rank + sub.dst_vpages // 8
+    single = di.AttnCase(B=6, T=1, H=64, n_dcp=1, dtype="e4m3", seq_lens=sub.seq_lens, req_page_ptr=sub.req_page_ptr,
+                         dst_vpages=vp.to(torch.int32), q=sub.q, pools=[one], slots_per_rank=8 * sub.slots_per_rank,
+                         kv_scale=sub.kv_scale, name="agent-6-dcp1")
+    o1, l1, _, _ = _run_attention(single)
+    compare(om.reshape(-1, 512), lm.reshape(-1), o1[0].reshape(-1, 512).astype(np.float64),
+            l1[0].reshape(-1).astype(np.float64), "DCP=1 vs DCP=8 merged")
+
+
+def test_attention_long_eagle_full_size_sampled(cuda_device):
+    """4 x 1,048,576 tokens, q_len 4 causal, FP8, DCP=8; sampled rows incl. every new token."""
+    case = di.long_eagle_case(cuda_device)
+    _sampled(case, *_run_attention(case), n_rows=12, ranks=(3,))
