@@ -24,7 +24,7 @@
 //    512 latent dims of the same pages (an L2 hit) into a 2-unit ring for P*V.  Separate
 //    MMA-issuing threads for the two products keep HBM loads in flight while the softmax
 //    of an earlier tile runs.
-//  * Eight softmax warps (two warpgroups of 32 query columns each) own one token row per
+//  * Sixteen softmax warps (four warpgroups of 16 query columns each) own one token row per
 //    thread (TMEM lane = row): scores are masked
 //    (ragged last page, causal limit among the new tokens), column maxima are reduced with a
 //    warp-shuffle reduce-scatter plus shared memory, exp2 weights go to shared memory, and
@@ -49,25 +49,31 @@
 namespace dcp {
 namespace {
 
-constexpr int kKSlots = 4;               // K-stream ring: 16 KB slots
+constexpr uint32_t kKSlotBytes = 16384;  // K-stream ring slot
 constexpr int kVSlots = 2;               // V-stream ring: 32 KB units
-constexpr uint32_t kKSlotBytes = 16384;
 constexpr uint32_t kVSlotBytes = 32768;
 constexpr uint32_t kQBytes = 73728;      // 64 rows x 576 BF16, or 128 rows (hi, lo) x 576 E4M3
-constexpr uint32_t kPBytes = 16384;
+constexpr uint32_t kPBytes = 16384;      // one P^T buffer
 constexpr int kGroupRows = 64;
-constexpr uint32_t kOffV = kKSlots * kKSlotBytes;
-constexpr uint32_t kOffQ = kOffV + kVSlots * kVSlotBytes;
-constexpr uint32_t kOffP = kOffQ + kQBytes;
-constexpr uint32_t kOffCtl = kOffP + kPBytes;
-constexpr int kThreads = 384;            // 0 K-TMA, 1 S-MMA, 2 V-TMA, 3 PV-MMA, 4-11 softmax
+constexpr int kThreads = 640;            // 0 K-TMA, 1 S-MMA, 2 V-TMA, 3 PV-MMA, 4-19 softmax
+constexpr int kCols = 16;                // query columns per softmax warpgroup
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 256;          // S buffers start at TMEM column 256 (O^T uses 0..255)
 constexpr int kMaxTpc = 4096;
-constexpr float kPScale = 256.f;         // FP8 P is stored as 256 * p (E4M3 range 448)
+
+constexpr float kPScale = 4.f;           // FP8 P is stored as 4 * p (p <= 2^6 under the lazy max)
 
 template <bool F8>
 struct Cfg {
+    // Four K slots and one P buffer (measured: trading a K slot for a second P buffer is
+    // slower for both element types).
+    static constexpr int kKSlots = 4;
+    static constexpr int kPBufs = 1;
+    static constexpr uint32_t kOffV = kKSlots * kKSlotBytes;
+    static constexpr uint32_t kOffQ = kOffV + kVSlots * kVSlotBytes;
+    static constexpr uint32_t kOffP = kOffQ + kQBytes;
+    static constexpr uint32_t kOffCtl = kOffP + kPBufs * kPBytes;
+    static constexpr float kLazyTauV = F8 ? 6.f : 8.f;  // log2 margin of the lazy maximum
     static constexpr int kKBlocks = F8 ? 5 : 9;     // K-stream blocks per tile
     static constexpr int kVUnits = F8 ? 2 : 4;      // V-stream units per tile
     static constexpr int kSCols = F8 ? 128 : 64;    // TMEM columns per S buffer (hi, lo for FP8)
@@ -84,24 +90,25 @@ struct UnitInfo {
 };
 
 struct __align__(16) Ctl {
-    float red[2][4][32];
+    float red[4][4][16];
     float m_run[64];
     float corr[64];
     float oscale[64];
     float qscale[64];            // per query row: softmax_scale * kappa * log2(e) * 2^-qexp
-    uint64_t kfull[kKSlots], kempty[kKSlots];
+    uint64_t kfull[4], kempty[4];
     uint64_t vfull[kVSlots], vempty[kVSlots];
     uint64_t q_full, q_empty;
     uint64_t s_full[3], s_free[3];
-    uint64_t p_full, o_done, o_free;
+    uint64_t p_full, o_done[2], o_free;
     uint64_t unit_full[2], unit_empty[2];
     uint64_t drain_s, drain_pv;
     UnitInfo unit[2];
     uint32_t tmem_base;
     int abort_flag;
 };
-constexpr size_t kSmemBytes = 1024 + kOffCtl + sizeof(Ctl);
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+template <bool F8>
+constexpr size_t smem_bytes() { return 1024 + Cfg<F8>::kOffCtl + sizeof(Ctl); }
+static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448, "shared memory budget");
 
 struct AttnMaps {
     CUtensorMap q[2];                  // BF16: [0] 64x64 boxes.  FP8 (hi|lo rows): [0] 128x64 SW128, [1] 64x64 SW64
@@ -133,6 +140,34 @@ struct KParams {
 // instead of 32 x 5 for a plain butterfly).
 template <bool kMax>
 __device__ __forceinline__ float rs_op(float a, float b) { return kMax ? fmaxf(a, b) : a + b; }
+
+// Same for 16 columns: lanes 2c and 2c+1 both return column c's reduction (16 shuffles).
+template <bool kMax>
+__device__ __forceinline__ float reduce_scatter16(const float (&v)[16], int lane) {
+    float r[8];
+    {
+        const bool upper = (lane & 16) != 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float send = upper ? v[i] : v[i + 8];
+            const float keep = upper ? v[i + 8] : v[i];
+            r[i] = rs_op<kMax>(keep, __shfl_xor_sync(0xffffffffu, send, 16));
+        }
+    }
+#pragma unroll
+    for (int half = 4, off = 8; half >= 1; half >>= 1, off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (i < half) {
+                const float send = upper ? r[i] : r[i + half];
+                const float keep = upper ? r[i + half] : r[i];
+                r[i] = rs_op<kMax>(keep, __shfl_xor_sync(0xffffffffu, send, off));
+            }
+        }
+    }
+    return rs_op<kMax>(r[0], __shfl_xor_sync(0xffffffffu, r[0], 1));
+}
 
 template <bool kMax>
 __device__ __forceinline__ float reduce_scatter32(const float (&v)[32], int lane) {
@@ -242,13 +277,15 @@ template <bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
 attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KParams p) {
     using C = Cfg<F8>;
+    constexpr float kLazyTau = C::kLazyTauV;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *kring = base;
-    uint8_t *vring = base + kOffV;
-    uint8_t *sq = base + kOffQ;
-    uint8_t *sp = base + kOffP;
-    Ctl *ctl = reinterpret_cast<Ctl *>(base + kOffCtl);
+    uint8_t *vring = base + C::kOffV;
+    uint8_t *sq = base + C::kOffQ;
+    uint8_t *sp = base + C::kOffP;
+    Ctl *ctl = reinterpret_cast<Ctl *>(base + C::kOffCtl);
+    constexpr int kKSlots = C::kKSlots;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     volatile int *abort_flag = &ctl->abort_flag;
     const uint64_t lim = p.wait_limit_ns;
@@ -266,15 +303,16 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
         mbar_init(&ctl->q_empty, 1);
         for (int i = 0; i < 3; ++i) {
             mbar_init(&ctl->s_full[i], 1);
-            mbar_init(&ctl->s_free[i], 256);
+            mbar_init(&ctl->s_free[i], 512);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctl->unit_full[i], 1);
-            mbar_init(&ctl->unit_empty[i], 5);
+            mbar_init(&ctl->unit_empty[i], 7);
         }
-        mbar_init(&ctl->p_full, 256);
-        mbar_init(&ctl->o_done, 1);
-        mbar_init(&ctl->o_free, 256);
+        mbar_init(&ctl->p_full, 512);
+        mbar_init(&ctl->o_done[0], 1);
+        mbar_init(&ctl->o_done[1], 1);
+        mbar_init(&ctl->o_free, 512);
         mbar_init(&ctl->drain_s, 1);
         mbar_init(&ctl->drain_pv, 1);
         ctl->abort_flag = 0;
@@ -509,7 +547,8 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                         ok = false;
                         break;
                     }
-                    ++p_cnt;
+                    const uint32_t tile_g = p_cnt++;  // global tile index: P buffer, o_done parity
+                    const uint32_t pb = p_addr + (tile_g % C::kPBufs) * kPBytes;
                     if (i == 0 && had_tiles) {
                         if (!mbar_wait(&ctl->o_free, of_cnt & 1, abort_flag, p.dev_error, lim)) {
                             ok = false;
@@ -534,9 +573,9 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk) {
                                     const uint64_t ad = smem_desc(a0 + h * 16384 + kk * 4096, 16384, 1024, kSwizzle128);
-                                    mma_f8_ss(d_tmem, ad, smem_desc(p_addr + kk * 2048, 512, 512, kSwizzle64),
+                                    mma_f8_ss(d_tmem, ad, smem_desc(pb + kk * 2048, 512, 512, kSwizzle64),
                                               C::kIdescPV, !(i == 0 && kk == 0));
-                                    mma_f8_ss(d_tmem, ad, smem_desc(p_addr + 8192 + kk * 2048, 512, 512, kSwizzle64),
+                                    mma_f8_ss(d_tmem, ad, smem_desc(pb + 8192 + kk * 2048, 512, 512, kSwizzle64),
                                               C::kIdescPV, 1);
                                 }
                             }
@@ -545,13 +584,13 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
 #pragma unroll
                             for (int kk = 0; kk < 8; ++kk)
                                 mma_f16_ss(d_tmem, smem_desc(a0 + kk * 2048, 16384, 1024, kSwizzle128),
-                                           smem_desc(p_addr + kk * 2048, 1024, 1024, kSwizzle128), C::kIdescPV,
+                                           smem_desc(pb + kk * 2048, 1024, 1024, kSwizzle128), C::kIdescPV,
                                            !(i == 0 && kk == 0));
                         }
                         mma_commit(&ctl->vempty[slot]);
                     }
                     if (!ok) break;
-                    mma_commit(&ctl->o_done);
+                    mma_commit(&ctl->o_done[tile_g & 1]);
                 }
                 had_tiles = true;
             }
@@ -561,16 +600,26 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
         }
     } else {
         // ---------------------------------------------------------------- softmax warps
-        // Two independent warpgroups; warpgroup g owns query columns [32g, 32g + 32) of every
+        // Four independent warpgroups; warpgroup g owns query columns [16g, 16g + 16) of every
         // tile.  Within a warpgroup each thread owns one token row (TMEM lane).
-        const int wg = (warp - 4) >> 2;             // 0 or 1
+        const int wg = (warp - 4) >> 2;             // 0..3
         const int gtid = threadIdx.x - 128 - 128 * wg;  // 0..127 within the warpgroup
         const int quad = warp & 3;                  // TMEM lane quadrant of this warp
         const int row = quad * 32 + lane;           // token row of the tile = TMEM lane
-        const int c0 = 32 * wg;                     // first query column of this warpgroup
+        const int c0 = kCols * wg;                  // first query column of this warpgroup
         const int bar_a = 1 + 2 * wg, bar_b = 2 + 2 * wg;
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        uint32_t s_cnt = 0, od_cnt = 0, k = 0;
+        uint32_t s_cnt = 0, obs_all = 0, k = 0;
+        // P*V of global tile t commits o_done[t & 1]; completions are observed strictly in tile
+        // order, so a barrier can never complete twice between two observations.
+        auto wait_pv = [&](uint32_t t) -> bool {
+            while (obs_all <= t) {
+                if (!warp_wait(&ctl->o_done[obs_all & 1], (obs_all >> 1) & 1, abort_flag, p.dev_error, lim))
+                    return false;
+                ++obs_all;
+            }
+            return true;
+        };
         while (true) {
             const int e = k & 1;
             int fail = !warp_wait(&ctl->unit_full[e], (k >> 1) & 1, abort_flag, p.dev_error, lim);
@@ -588,27 +637,32 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
             float *obase = direct ? p.o_part : p.part_o;
             float *lbase = direct ? p.lse_part : p.part_lse;
             if (nt == 0) {
-                for (int idx = gtid; idx < 32 * (kVDim / 4); idx += 128) {
+                for (int idx = gtid; idx < kCols * (kVDim / 4); idx += 128) {
                     const int c = c0 + idx / (kVDim / 4), v4 = idx % (kVDim / 4);
                     if (c < u.rows_valid)
                         reinterpret_cast<float4 *>(obase + (out_row0 + c) * kVDim)[v4] = make_float4(0.f, 0.f, 0.f, 0.f);
                 }
-                if (gtid < 32 && c0 + gtid < u.rows_valid) lbase[out_row0 + c0 + gtid] = -INFINITY;
+                if (gtid < kCols && c0 + gtid < u.rows_valid) lbase[out_row0 + c0 + gtid] = -INFINITY;
                 continue;
             }
-            if (gtid < 32) {
-                ctl->m_run[c0 + gtid] = -INFINITY;
+            // Per-column score scale and reference maximum, kept in registers.  The reference
+            // trails the true running maximum by at most kLazyTau (log2 units): a tile whose
+            // scores all stay within that margin is exponentiated against the old reference
+            // (weights up to 2^kLazyTau, exact after the final normalisation) and skips the
+            // cross-thread maximum and the O rescale.
+            float qsr[kCols], mref[kCols], lp[kCols];
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) {
                 float qs = p.sl2;
                 if (F8) {
-                    const int qr = u.q_row0 + c0 + gtid;
-                    qs *= (qr < p.R) ? p.q_rscale[qr] : 0.f;
+                    const int qr = u.q_row0 + c0 + c;
+                    qs *= (qr < p.R) ? __ldg(p.q_rscale + qr) : 0.f;
                 }
-                ctl->qscale[c0 + gtid] = qs;
+                qsr[c] = qs;
+                mref[c] = -INFINITY;
+                lp[c] = 0.f;
             }
-            named_bar_sync(bar_b, 128);
-            float lp[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) lp[c] = 0.f;
+            if (gtid < kCols) ctl->m_run[c0 + gtid] = -INFINITY;
             // page index of this row's page in tile 0, then prefetched one tile ahead
             int j_cur = -1;
             {
@@ -622,20 +676,22 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     const int pl = 2 * (i + 1) + (row >> 6);
                     if (i + 1 < nt && pl < u.n_pages) j_next = p.comp_page[u.comp_base + pl];
                 }
+                const uint32_t g = s_cnt;  // global tile index
                 const uint32_t sb = s_cnt % C::kSBufs;
                 fail = !warp_wait(&ctl->s_full[sb], (s_cnt / C::kSBufs) & 1, abort_flag, p.dev_error, lim);
                 ++s_cnt;
-                float s[32];
+                float s[kCols];
+                int over = 0;
                 if (!fail) {
                     tc_fence_after();
                     const uint32_t ta = tmem + lane_base + kSCol + C::kSCols * sb + c0;
-                    tmem_ld32(ta, s);
+                    tmem_ld16(ta, s);
                     if (F8) {
-                        float t32[32];
-                        tmem_ld32(ta + 64, t32);
+                        float t[kCols];
+                        tmem_ld16(ta + 64, t);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) s[c] += t32[c];
+                        for (int c = 0; c < kCols; ++c) s[c] += t[c];
                     } else {
                         tmem_wait_ld();
                     }
@@ -644,96 +700,91 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     // mask: ragged last page / missing second page / causal limit
                     const bool valid = j_cur >= 0 && (long long)j_cur * 64 + (row & 63) <= (long long)u.limit;
 #pragma unroll
-                    for (int c = 0; c < 32; c += 4) {
-                        const float4 q4 = *reinterpret_cast<const float4 *>(&ctl->qscale[c0 + c]);
-                        s[c] = valid ? s[c] * q4.x : -INFINITY;
-                        s[c + 1] = valid ? s[c + 1] * q4.y : -INFINITY;
-                        s[c + 2] = valid ? s[c + 2] * q4.z : -INFINITY;
-                        s[c + 3] = valid ? s[c + 3] * q4.w : -INFINITY;
+                    for (int c = 0; c < kCols; ++c) {
+                        s[c] = valid ? s[c] * qsr[c] : -INFINITY;
+                        over |= s[c] > mref[c] + kLazyTau;
                     }
-                    const float r = reduce_scatter32<true>(s, lane);
-                    ctl->red[wg][quad][lane] = r;
                 }
                 j_cur = j_next;
-                if (named_bar_or(bar_a, 128, fail)) {
-                    aborted = true;
-                    break;
-                }
-                int changed = 0;
-                if (gtid < 32) {
-                    const int c = c0 + gtid;
-                    const float mt = fmaxf(fmaxf(ctl->red[wg][0][gtid], ctl->red[wg][1][gtid]),
-                                           fmaxf(ctl->red[wg][2][gtid], ctl->red[wg][3][gtid]));
-                    const float mo = ctl->m_run[c];
-                    const float mn = fmaxf(mo, mt);
-                    const float cr = (mn == mo) ? 1.f : fast_exp2(mo - mn);
-                    ctl->m_run[c] = mn;
-                    ctl->corr[c] = cr;
-                    changed = cr != 1.f;
-                }
-                const int any = named_bar_or(bar_b, 128, changed);
-#pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const float4 m4 = *reinterpret_cast<const float4 *>(&ctl->m_run[c0 + c]);
-                    float4 c4 = make_float4(1.f, 1.f, 1.f, 1.f);
-                    if (any) c4 = *reinterpret_cast<const float4 *>(&ctl->corr[c0 + c]);
-                    const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-                    const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const float ms = mm[q] == -INFINITY ? 0.f : mm[q];
-                        s[c + q] = fast_exp2(s[c + q] - ms);
-                        lp[c + q] = fmaf(lp[c + q], cc[q], s[c + q]);
+                if (named_bar_or(bar_a, 128, fail | over)) {
+                    if (named_bar_or(bar_b, 128, fail)) {
+                        aborted = true;
+                        break;
                     }
-                }
-                if (i > 0) {
-                    fail = !warp_wait(&ctl->o_done, od_cnt & 1, abort_flag, p.dev_error, lim);
-                    ++od_cnt;
-                    if (fail) continue;  // the next OR-barrier takes the warpgroup out
-                    tc_fence_after();
-                    if (any) {
+                    // slow path: exact column maxima of this tile, new references, rescale
+                    const float r = reduce_scatter16<true>(s, lane);
+                    if ((lane & 1) == 0) ctl->red[wg][quad][lane >> 1] = r;
+                    named_bar_sync(bar_a, 128);
+                    if (gtid < kCols) {
+                        const int c = c0 + gtid;
+                        const float mt = fmaxf(fmaxf(ctl->red[wg][0][gtid], ctl->red[wg][1][gtid]),
+                                               fmaxf(ctl->red[wg][2][gtid], ctl->red[wg][3][gtid]));
+                        const float mo = ctl->m_run[c];
+                        const float mn = fmaxf(mo, mt);
+                        ctl->m_run[c] = mn;
+                        ctl->corr[c] = (mn == mo) ? 1.f : fast_exp2(mo - mn);
+                    }
+                    named_bar_sync(bar_b, 128);
+                    float cr[kCols];
+#pragma unroll
+                    for (int c = 0; c < kCols; ++c) {
+                        mref[c] = ctl->m_run[c0 + c];
+                        cr[c] = ctl->corr[c0 + c];
+                        lp[c] *= cr[c];
+                    }
+                    if (i > 0) {  // the rescale needs P*V of the previous tile complete
+                        fail = !wait_pv(g - 1);
+                        if (fail) continue;  // the next OR-barrier takes the warpgroup out
+                        tc_fence_after();
 #pragma unroll 1
                         for (int j = 0; j < 4; ++j) {
-                            float o32[32];
+                            float o[kCols];
                             const uint32_t ta = tmem + lane_base + 64 * j + c0;
-                            tmem_ld32(ta, o32);
+                            tmem_ld16(ta, o);
                             tmem_wait_ld();
 #pragma unroll
-                            for (int c = 0; c < 32; ++c) o32[c] *= ctl->corr[c0 + c];
-                            tmem_st32(ta, o32);
+                            for (int c = 0; c < kCols; ++c) o[c] *= cr[c];
+                            tmem_st16(ta, o);
                         }
                         tmem_wait_st();
                     }
                 }
+                if (g >= (uint32_t)C::kPBufs) {  // P buffer g % kPBufs: its previous reader must be done
+                    fail = !wait_pv(g - C::kPBufs);
+                    if (fail) continue;
+                    tc_fence_after();
+                }
+#pragma unroll
+                for (int c = 0; c < kCols; ++c) {
+                    const float ms = mref[c] == -INFINITY ? 0.f : mref[c];
+                    s[c] = fast_exp2(s[c] - ms);
+                    lp[c] += s[c];
+                }
                 if (F8) {
                     // P^T row as hi and lo E4M3 rows of 64 bytes, MN-major, 64-byte swizzle;
-                    // this warpgroup writes 16-byte chunks 2wg and 2wg + 1 of each.
+                    // this warpgroup writes 16-byte chunk wg of each.
                     const uint32_t off = (row >> 3) * 512 + (row & 7) * 64;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint4 hv, lv;
-                        const float *v = s + 16 * h;
-                        split_e4m3x4(v[0] * kPScale, v[1] * kPScale, v[2] * kPScale, v[3] * kPScale, hv.x, lv.x);
-                        split_e4m3x4(v[4] * kPScale, v[5] * kPScale, v[6] * kPScale, v[7] * kPScale, hv.y, lv.y);
-                        split_e4m3x4(v[8] * kPScale, v[9] * kPScale, v[10] * kPScale, v[11] * kPScale, hv.z, lv.z);
-                        split_e4m3x4(v[12] * kPScale, v[13] * kPScale, v[14] * kPScale, v[15] * kPScale, hv.w, lv.w);
-                        const int cc = 2 * wg + h;
-                        const uint32_t sw = ((cc ^ ((row >> 1) & 3)) << 4);
-                        *reinterpret_cast<uint4 *>(sp + off + sw) = hv;
-                        *reinterpret_cast<uint4 *>(sp + 8192 + off + sw) = lv;
-                    }
+                    uint4 hv, lv;
+                    split_e4m3x4(s[0] * kPScale, s[1] * kPScale, s[2] * kPScale, s[3] * kPScale, hv.x, lv.x);
+                    split_e4m3x4(s[4] * kPScale, s[5] * kPScale, s[6] * kPScale, s[7] * kPScale, hv.y, lv.y);
+                    split_e4m3x4(s[8] * kPScale, s[9] * kPScale, s[10] * kPScale, s[11] * kPScale, hv.z, lv.z);
+                    split_e4m3x4(s[12] * kPScale, s[13] * kPScale, s[14] * kPScale, s[15] * kPScale, hv.w, lv.w);
+                    const uint32_t sw = ((wg ^ ((row >> 1) & 3)) << 4);
+                    uint8_t *pbuf = sp + (g % C::kPBufs) * kPBytes;
+                    *reinterpret_cast<uint4 *>(pbuf + off + sw) = hv;
+                    *reinterpret_cast<uint4 *>(pbuf + 8192 + off + sw) = lv;
                 } else {
                     // P^T row: 64 BF16 values, MN-major with the 128-byte swizzle; this
-                    // warpgroup writes 16-byte chunks 4wg .. 4wg + 3.
-                    uint8_t *prow = sp + (row >> 3) * 1024 + (row & 7) * 128;
+                    // warpgroup writes 16-byte chunks 2wg and 2wg + 1.
+                    uint8_t *prow = sp + (g % C::kPBufs) * kPBytes + (row >> 3) * 1024 + (row & 7) * 128;
 #pragma unroll
-                    for (int h = 0; h < 4; ++h) {
+                    for (int h = 0; h < 2; ++h) {
                         uint4 w;
                         w.x = pack_bf16(s[8 * h + 0], s[8 * h + 1]);
                         w.y = pack_bf16(s[8 * h + 2], s[8 * h + 3]);
                         w.z = pack_bf16(s[8 * h + 4], s[8 * h + 5]);
                         w.w = pack_bf16(s[8 * h + 6], s[8 * h + 7]);
-                        const int cc = 4 * wg + h;
+                        const int cc = 2 * wg + h;
                         *reinterpret_cast<uint4 *>(prow + ((cc ^ (row & 7)) << 4)) = w;
                     }
                 }
@@ -742,12 +793,14 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                 mbar_arrive(&ctl->p_full);
             }
             if (aborted) break;
-            fail = !warp_wait(&ctl->o_done, od_cnt & 1, abort_flag, p.dev_error, lim);
-            ++od_cnt;
+            fail = !wait_pv(s_cnt - 1);
             tc_fence_after();
-            ctl->red[wg][quad][lane] = reduce_scatter32<false>(lp, lane);
+            {
+                const float r = reduce_scatter16<false>(lp, lane);
+                if ((lane & 1) == 0) ctl->red[wg][quad][lane >> 1] = r;
+            }
             if (named_bar_or(bar_a, 128, fail)) break;
-            if (gtid < 32) {
+            if (gtid < kCols) {
                 const int c = c0 + gtid;
                 const float L = ctl->red[wg][0][gtid] + ctl->red[wg][1][gtid] + ctl->red[wg][2][gtid] +
                                 ctl->red[wg][3][gtid];
@@ -758,16 +811,19 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     lbase[out_row0 + c] = live ? (mr + log2f(L)) * 0.69314718055994531f : -INFINITY;
             }
             named_bar_sync(bar_b, 128);
+            float osc[kCols];
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) osc[c] = ctl->oscale[c0 + c];
 #pragma unroll 1
             for (int j = 0; j < 4; ++j) {
-                float o32[32];
-                tmem_ld32(tmem + lane_base + 64 * j + c0, o32);
+                float o[kCols];
+                tmem_ld16(tmem + lane_base + 64 * j + c0, o);
                 tmem_wait_ld();
                 const int vcol = j * 128 + row;  // V dimension held by this lane
 #pragma unroll
-                for (int c = 0; c < 32; ++c)
+                for (int c = 0; c < kCols; ++c)
                     if (c0 + c < u.rows_valid)
-                        obase[(out_row0 + c0 + c) * kVDim + vcol] = o32[c] * ctl->oscale[c0 + c];
+                        obase[(out_row0 + c0 + c) * kVDim + vcol] = o[c] * osc[c];
             }
             tc_fence_before();
             mbar_arrive(&ctl->o_free);
@@ -1034,10 +1090,10 @@ bool plan_attention(int B, int T, int H, int N, int64_t num_pages, int dtype, in
 
 template <bool F8>
 int launch_kernel(const AttnMaps &maps, const KParams &kp, int grid, cudaStream_t stream) {
-    if (cudaFuncSetAttribute(attn_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-        cudaSuccess)
+    constexpr size_t smem = smem_bytes<F8>();
+    if (cudaFuncSetAttribute(attn_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DCP_ERR_CUDA;
-    attn_kernel<F8><<<grid, kThreads, kSmemBytes, stream>>>(maps, kp);
+    attn_kernel<F8><<<grid, kThreads, smem, stream>>>(maps, kp);
     return cudaGetLastError() == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
 }
 
