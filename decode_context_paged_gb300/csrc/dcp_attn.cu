@@ -837,50 +837,87 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
 }
 
 // ------------------------------------------------------------------------------ plan
-// One warp per request: stable per-rank compaction of the request's pages.
-__global__ void plan_pages_kernel(int B, int N, long long num_pages, long long slots_per_rank,
-                                  const int64_t *__restrict__ req_page_ptr,
-                                  const int32_t *__restrict__ vpages, int32_t *__restrict__ counts,
-                                  int32_t *__restrict__ comp_slot, int32_t *__restrict__ comp_page,
-                                  int32_t *dev_error) {
-    const int lane = threadIdx.x & 31;
-    const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (b >= B) return;
-    const long long p0 = req_page_ptr[b], p1 = req_page_ptr[b + 1];
-    int cnt[kMaxDcpAttn];
-#pragma unroll
-    for (int d = 0; d < kMaxDcpAttn; ++d) cnt[d] = 0;
+// Per-rank compaction of every request's pages, in three parallel steps over tiles of 1024
+// pages of one request (grid x = tile within the request, grid y = request):
+//   plan_count_kernel   owner counts per tile;
+//   plan_units_kernel   per (rank, request): exclusive scan of the tile counts (tile bases)
+//                       and the total, then the unit list;
+//   plan_scatter_kernel each page to position base + stable in-tile rank among same-owner pages.
+// Rank d's pages of request b end up, in page order, at d * num_pages + req_page_ptr[b] + pos.
+constexpr int kPlanTile = 1024;
+constexpr int kPlanTileThreads = 256;
+
+__device__ __forceinline__ int page_owner_slot(int v, int N, long long slots_per_rank, int &slot) {
+    const int d = N <= 1 ? 0 : v % N;
+    const long long s = N <= 1 ? (long long)v : (long long)(v / N);
+    if (v < 0 || s >= slots_per_rank) return -1;
+    slot = (int)s;
+    return d;
+}
+
+__global__ void __launch_bounds__(kPlanTileThreads)
+plan_count_kernel(int N, long long slots_per_rank, int tiles_per_req, const int64_t *__restrict__ req_page_ptr,
+                  const int32_t *__restrict__ vpages, int32_t *__restrict__ tile_cnt, int32_t *dev_error) {
+    __shared__ int cnt[kMaxDcpAttn];
+    const int b = blockIdx.y, k = blockIdx.x;
+    const long long p0 = req_page_ptr[b] + (long long)k * kPlanTile, p1 = req_page_ptr[b + 1];
+    if (threadIdx.x < kMaxDcpAttn) cnt[threadIdx.x] = 0;
+    __syncthreads();
     bool bad = false;
-    for (long long base = p0; base < p1; base += 32) {
-        const long long i = base + lane;
-        int d = -1;
-        int slot = 0;
+    for (int e = 0; e < kPlanTile / kPlanTileThreads; ++e) {
+        const long long i = p0 + e * kPlanTileThreads + threadIdx.x;
         if (i < p1) {
-            const int v = vpages[i];
-            const int dd = N <= 1 ? 0 : v % N;
-            const long long s = N <= 1 ? (long long)v : (long long)(v / N);
-            if (v < 0 || s >= slots_per_rank) {
-                bad = true;
-            } else {
-                d = dd;
-                slot = (int)s;
-            }
-        }
-#pragma unroll
-        for (int dd = 0; dd < kMaxDcpAttn; ++dd) {
-            if (dd >= N) break;
-            const unsigned m = __ballot_sync(0xffffffffu, d == dd);
-            if (d == dd) {
-                const long long pos = (long long)dd * num_pages + p0 + cnt[dd] + __popc(m & ((1u << lane) - 1u));
-                comp_slot[pos] = slot;
-                comp_page[pos] = (int)(i - p0);
-            }
-            cnt[dd] += __popc(m);
+            int slot;
+            const int d = page_owner_slot(vpages[i], N, slots_per_rank, slot);
+            if (d < 0) bad = true;
+            else atomicAdd(&cnt[d], 1);
         }
     }
+    __syncthreads();
+    if (p0 < p1 && threadIdx.x < N) tile_cnt[((long long)b * tiles_per_req + k) * kMaxDcpAttn + threadIdx.x] = cnt[threadIdx.x];
     if (bad && dev_error) atomicOr(dev_error, DCP_DEVERR_OUT_OF_RANGE);
-    if (lane == 0)
-        for (int d = 0; d < N; ++d) counts[d * B + b] = cnt[d];
+}
+
+__global__ void __launch_bounds__(kPlanTileThreads)
+plan_scatter_kernel(int N, long long num_pages, long long slots_per_rank, int tiles_per_req,
+                    const int64_t *__restrict__ req_page_ptr, const int32_t *__restrict__ vpages,
+                    const int32_t *__restrict__ tile_base, int32_t *__restrict__ comp_slot,
+                    int32_t *__restrict__ comp_page) {
+    __shared__ int wcnt[kPlanTileThreads / 32][kMaxDcpAttn];
+    __shared__ int run[kMaxDcpAttn];
+    const int b = blockIdx.y, k = blockIdx.x;
+    const long long r0 = req_page_ptr[b];
+    const long long p0 = r0 + (long long)k * kPlanTile, p1 = req_page_ptr[b + 1];
+    if (p0 >= p1) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (threadIdx.x < kMaxDcpAttn)
+        run[threadIdx.x] = threadIdx.x < N ? tile_base[((long long)b * tiles_per_req + k) * kMaxDcpAttn + threadIdx.x] : 0;
+    for (int e = 0; e < kPlanTile / kPlanTileThreads; ++e) {
+        const long long i = p0 + e * kPlanTileThreads + threadIdx.x;
+        int d = -1, slot = 0;
+        if (i < p1) d = page_owner_slot(vpages[i], N, slots_per_rank, slot);
+        int my_rank_in_warp = 0;
+        for (int dd = 0; dd < N; ++dd) {
+            const unsigned m = __ballot_sync(0xffffffffu, d == dd);
+            if (lane == 0) wcnt[warp][dd] = __popc(m);
+            if (d == dd) my_rank_in_warp = __popc(m & ((1u << lane) - 1u));
+        }
+        __syncthreads();
+        if (d >= 0) {
+            int before = run[d];
+            for (int w = 0; w < warp; ++w) before += wcnt[w][d];
+            const long long pos = (long long)d * num_pages + r0 + before + my_rank_in_warp;
+            comp_slot[pos] = slot;
+            comp_page[pos] = (int)(i - r0);
+        }
+        __syncthreads();
+        if (threadIdx.x < N) {
+            int t = 0;
+            for (int w = 0; w < kPlanTileThreads / 32; ++w) t += wcnt[w][threadIdx.x];
+            run[threadIdx.x] += t;
+        }
+        __syncthreads();
+    }
 }
 
 // Single block: chunk each (rank, request) pair, assign partial slots, emit units largest
@@ -916,12 +953,28 @@ __device__ long long block_exclusive_scan(long long x, long long *scratch, long 
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
-plan_units_kernel(int B, int N, int G, int only_rank, int tpc, const int32_t *__restrict__ counts,
-                  int32_t *__restrict__ pair_chunks, int32_t *__restrict__ pair_part,
+plan_units_kernel(int B, int N, int G, int only_rank, int tpc, const int64_t *__restrict__ req_page_ptr,
+                  int tiles_per_req, const int32_t *__restrict__ tile_cnt, int32_t *__restrict__ tile_base,
+                  int32_t *__restrict__ counts, int32_t *__restrict__ pair_chunks, int32_t *__restrict__ pair_part,
                   int4 *__restrict__ units, int *__restrict__ ctrl) {
     __shared__ int hist[kMaxTpc + 1];
     __shared__ long long scratch[33];
     const int n_pair = N * B;
+    // per (rank, request): exclusive scan of the tile counts and the total
+    for (int pr = threadIdx.x; pr < n_pair; pr += kPlanThreads) {
+        const int d = pr / B, b = pr % B;
+        const long long np = req_page_ptr[b + 1] - req_page_ptr[b];
+        const int nt = (int)((np + kPlanTile - 1) / kPlanTile);
+        int acc = 0;
+        for (int k = 0; k < nt; ++k) {
+            const long long ix = ((long long)b * tiles_per_req + k) * kMaxDcpAttn + d;
+            const int c = tile_cnt[ix];
+            tile_base[ix] = acc;
+            acc += c;
+        }
+        counts[pr] = acc;
+    }
+    __syncthreads();
     for (int i = threadIdx.x; i <= tpc; i += kPlanThreads) hist[i] = 0;
     __syncthreads();
     long long running = 0;
@@ -1079,6 +1132,8 @@ bool plan_attention(int B, int T, int H, int N, int64_t num_pages, int dtype, in
     s->off_units = off;   off = align256(off + sizeof(int4) * (size_t)s->max_units);
     s->off_seg = off;     off = align256(off + sizeof(int32_t) * 2 * (size_t)N * B);
     s->off_ctrl = off;    off = align256(off + sizeof(int32_t) * 4);
+    s->tiles_per_req = (int)std::max<long long>(1, (num_pages + kPlanTile - 1) / kPlanTile);
+    s->off_tiles = off;   off = align256(off + sizeof(int32_t) * 2 * (size_t)B * s->tiles_per_req * kMaxDcpAttn);
     s->off_part_o = off;  off = align256(off + sizeof(float) * (size_t)s->max_partials * kGroupRows * kVDim);
     s->off_part_lse = off; off = align256(off + sizeof(float) * (size_t)s->max_partials * kGroupRows);
     const size_t R = (size_t)B * T * H;
@@ -1115,14 +1170,24 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     float *qscale = reinterpret_cast<float *>(ws + s.off_qscale);
     const int R = s.B * s.T * s.H;
 
-    const int warps_per_block = 4;
-    plan_pages_kernel<<<(s.B + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, stream>>>(
-        s.B, s.N, s.num_pages, a.slots_per_rank, a.req_page_ptr, a.dst_vpages, counts, comp_slot, comp_page,
-        a.dev_error);
+    int32_t *tile_cnt = reinterpret_cast<int32_t *>(ws + s.off_tiles);
+    int32_t *tile_base = tile_cnt + (size_t)s.B * s.tiles_per_req * kMaxDcpAttn;
+    const dim3 tgrid((unsigned)s.tiles_per_req, (unsigned)s.B);
+    if (s.num_pages > 0) {
+        plan_count_kernel<<<tgrid, kPlanTileThreads, 0, stream>>>(s.N, a.slots_per_rank, s.tiles_per_req,
+                                                                   a.req_page_ptr, a.dst_vpages, tile_cnt, a.dev_error);
+        if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
+    }
+    plan_units_kernel<<<1, kPlanThreads, 0, stream>>>(s.B, s.N, s.G, a.only_rank, s.tiles_per_chunk, a.req_page_ptr,
+                                                       s.tiles_per_req, tile_cnt, tile_base, counts, pair_chunks,
+                                                       pair_part, units, ctrl);
     if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
-    plan_units_kernel<<<1, kPlanThreads, 0, stream>>>(s.B, s.N, s.G, a.only_rank, s.tiles_per_chunk, counts,
-                                                       pair_chunks, pair_part, units, ctrl);
-    if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
+    if (s.num_pages > 0) {
+        plan_scatter_kernel<<<tgrid, kPlanTileThreads, 0, stream>>>(s.N, s.num_pages, a.slots_per_rank,
+                                                                     s.tiles_per_req, a.req_page_ptr, a.dst_vpages,
+                                                                     tile_base, comp_slot, comp_page);
+        if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
+    }
     if (f8) {
         q_split_kernel<<<(R + 7) / 8, 256, 0, stream>>>(R, reinterpret_cast<const __nv_bfloat16 *>(a.q), qhl, qscale);
         if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;

@@ -61,7 +61,8 @@ struct AttnPlanShape {
     int64_t max_partials;
     int64_t n_seg;
     size_t off_counts, off_slots, off_pages, off_units, off_seg, off_ctrl, off_part_o,
-        off_part_lse, off_qhl, off_qscale;
+        off_part_lse, off_qhl, off_qscale, off_tiles;
+    int tiles_per_req;
     size_t total_bytes;
 };
 bool plan_attention(int B, int T, int H, int N, int64_t num_pages, int dtype, int num_sms,
