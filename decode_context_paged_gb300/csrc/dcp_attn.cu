@@ -62,6 +62,11 @@ constexpr uint32_t kSCol = 256;          // S buffers start at TMEM column 256 (
 constexpr int kMaxTpc = 4096;
 
 constexpr float kPScale = 4.f;           // FP8 P is stored as 4 * p (p <= 2^6 under the lazy max)
+// FP8 P is split into E4M3 hi + lo terms unless the (rank, request) segment has at least this
+// many pages (8192 tokens).  One E4M3 term carries a relative rounding error of up to 2^-4 per
+// weight; its effect on O shrinks like 1/sqrt(effective number of keys), which for segments
+// this long stays far below the output tolerance, while short segments keep the lo term.
+constexpr int kSinglePMinPages = 128;
 
 template <bool F8>
 struct Cfg {
@@ -85,7 +90,7 @@ struct Cfg {
 struct UnitInfo {
     int valid, d, b, g;
     int n_pages, out_index, limit, q_row0;
-    int rows_valid, pad0;
+    int rows_valid, p_single;  // p_single: FP8 P as one E4M3 term (no lo term)
     long long comp_base;
 };
 
@@ -213,6 +218,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+
+// Four values to E4M3 (round to nearest even, saturating), packed little-endian.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+    const __nv_fp8x2_storage_t p01 = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const __nv_fp8x2_storage_t p23 = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return (uint32_t)p01 | ((uint32_t)p23 << 16);
 }
 
 // E4M3 hi/lo split of 4 values (already scaled into range): hi = e4m3(x), lo = e4m3(x - hi).
@@ -368,7 +380,8 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     u.d = pair / p.B;
                     u.b = pair - u.d * p.B;
                     const int t = u.g / p.HB, hb = u.g - (u.g / p.HB) * p.HB;
-                    u.n_pages = rec.z;
+                    u.n_pages = rec.z & 0x3FFFFFFF;
+                    u.p_single = (rec.z >> 30) & 1;
                     u.out_index = rec.w;
                     u.limit = p.seq_lens[u.b] - p.T + t;
                     u.q_row0 = (u.b * p.T + t) * p.H + hb * kGroupRows;
@@ -575,8 +588,9 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                                     const uint64_t ad = smem_desc(a0 + h * 16384 + kk * 4096, 16384, 1024, kSwizzle128);
                                     mma_f8_ss(d_tmem, ad, smem_desc(pb + kk * 2048, 512, 512, kSwizzle64),
                                               C::kIdescPV, !(i == 0 && kk == 0));
-                                    mma_f8_ss(d_tmem, ad, smem_desc(pb + 8192 + kk * 2048, 512, 512, kSwizzle64),
-                                              C::kIdescPV, 1);
+                                    if (!u.p_single)
+                                        mma_f8_ss(d_tmem, ad, smem_desc(pb + 8192 + kk * 2048, 512, 512, kSwizzle64),
+                                                  C::kIdescPV, 1);
                                 }
                             }
                         } else {
@@ -764,15 +778,24 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     // P^T row as hi and lo E4M3 rows of 64 bytes, MN-major, 64-byte swizzle;
                     // this warpgroup writes 16-byte chunk wg of each.
                     const uint32_t off = (row >> 3) * 512 + (row & 7) * 64;
-                    uint4 hv, lv;
-                    split_e4m3x4(s[0] * kPScale, s[1] * kPScale, s[2] * kPScale, s[3] * kPScale, hv.x, lv.x);
-                    split_e4m3x4(s[4] * kPScale, s[5] * kPScale, s[6] * kPScale, s[7] * kPScale, hv.y, lv.y);
-                    split_e4m3x4(s[8] * kPScale, s[9] * kPScale, s[10] * kPScale, s[11] * kPScale, hv.z, lv.z);
-                    split_e4m3x4(s[12] * kPScale, s[13] * kPScale, s[14] * kPScale, s[15] * kPScale, hv.w, lv.w);
                     const uint32_t sw = ((wg ^ ((row >> 1) & 3)) << 4);
                     uint8_t *pbuf = sp + (g % C::kPBufs) * kPBytes;
-                    *reinterpret_cast<uint4 *>(pbuf + off + sw) = hv;
-                    *reinterpret_cast<uint4 *>(pbuf + 8192 + off + sw) = lv;
+                    if (u.p_single) {
+                        uint4 hv;
+                        hv.x = e4m3x4(s[0] * kPScale, s[1] * kPScale, s[2] * kPScale, s[3] * kPScale);
+                        hv.y = e4m3x4(s[4] * kPScale, s[5] * kPScale, s[6] * kPScale, s[7] * kPScale);
+                        hv.z = e4m3x4(s[8] * kPScale, s[9] * kPScale, s[10] * kPScale, s[11] * kPScale);
+                        hv.w = e4m3x4(s[12] * kPScale, s[13] * kPScale, s[14] * kPScale, s[15] * kPScale);
+                        *reinterpret_cast<uint4 *>(pbuf + off + sw) = hv;
+                    } else {
+                        uint4 hv, lv;
+                        split_e4m3x4(s[0] * kPScale, s[1] * kPScale, s[2] * kPScale, s[3] * kPScale, hv.x, lv.x);
+                        split_e4m3x4(s[4] * kPScale, s[5] * kPScale, s[6] * kPScale, s[7] * kPScale, hv.y, lv.y);
+                        split_e4m3x4(s[8] * kPScale, s[9] * kPScale, s[10] * kPScale, s[11] * kPScale, hv.z, lv.z);
+                        split_e4m3x4(s[12] * kPScale, s[13] * kPScale, s[14] * kPScale, s[15] * kPScale, hv.w, lv.w);
+                        *reinterpret_cast<uint4 *>(pbuf + off + sw) = hv;
+                        *reinterpret_cast<uint4 *>(pbuf + 8192 + off + sw) = lv;
+                    }
                 } else {
                     // P^T row: 64 BF16 values, MN-major with the 128-byte swizzle; this
                     // warpgroup writes 16-byte chunks 2wg and 2wg + 1.
@@ -1023,7 +1046,8 @@ plan_units_kernel(int B, int N, int G, int only_rank, int tpc, const int64_t *__
             const int n_pages = max(0, min(2 * tpc, cnt - page_begin));
             for (int g = 0; g < G; ++g) {
                 const int out = chunks > 1 ? pair_part[pr] + c * G + g : -1;
-                units[(long long)slot * G + g] = make_int4(pr * G + g, page_begin, n_pages, out);
+                units[(long long)slot * G + g] =
+                    make_int4(pr * G + g, page_begin, n_pages | (cnt >= kSinglePMinPages ? (1 << 30) : 0), out);
             }
         }
     }

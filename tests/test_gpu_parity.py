@@ -151,6 +151,8 @@ ATTN_CASES = [
     ("empty-ranks-fp8", [64, 200, 1], 64, 1, 8, "e4m3"),
     ("causal-q4-fp8", [64 * 7 + 3, 66, 260], 64, 4, 2, "e4m3"),
     ("heads-96-fp8", [700, 333], 96, 1, 3, "e4m3"),
+    # one long segment per rank (single-term FP8 P) next to short ones (hi + lo P)
+    ("mixed-len-fp8", [70_000, 9_000], 64, 1, 8, "e4m3"),
 ]
 
 
