@@ -36,9 +36,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernels below on the default workload, with the hash of the kernel source they were taken
 # on; a changed source reports traffic null until it is re-measured.
 NCU_TRAFFIC = {
-    # (kernel, workload): (source hash, bytes per launch); profiles/attn_kernel__batch-32x8192-h64-bf16-dcp8.md
-    ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("37f38495550d4afc", 551839000),
-    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("49a82f8ae989d93b", 331932928),
+    # (kernel, workload): (source hash, DRAM bytes per launch)
+    ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("37f38495550d4afc", 552532480),
+    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("af4a93841d19dfbf", 327653120),
+    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("af4a93841d19dfbf", 3057132592),
 }
 
 
