@@ -165,8 +165,8 @@ class Workload:
         self.flops_attn = 2 * keys * self.H * (576 + 512) * self.L
         self.name = (f"{name}-{self.B}x{max(lens)}-h{self.H}-q{self.T}-{self.dtype}-dcp{self.N}"
                      + (f"-L{self.L}-cp{self.n_cp}" if self.L > 1 else ""))
-        # reshard + per layer: plan count, plan units, plan scatter, (Q split for FP8), attention, combine, merge
-        self.launches_per_step = 1 + self.L * (7 if self.dtype == "e4m3" else 6)
+        # reshard + per layer: plan count (+ FP8 Q split), plan build, attention, combine, merge
+        self.launches_per_step = 1 + self.L * 5
 
     def step(self, dcp, events=None):
         """events: dict stage -> list of (start, end) event pairs, appended per call."""

@@ -244,11 +244,9 @@ __device__ __forceinline__ void split_e4m3x4(float a, float b, float c, float d,
 // FP8 path: Q (BF16) -> hi and lo E4M3 rows scaled by a power of two per row so that the
 // row's largest magnitude lands in (224, 448]; q = (hi + lo) * 2^-qexp up to ~2^-8 relative.
 // One warp per query row.  Output rows [0, R) = hi, [R, 2R) = lo; rscale[row] = 2^-qexp.
-__global__ void q_split_kernel(int R, const __nv_bfloat16 *__restrict__ q, uint8_t *__restrict__ qhl,
-                               float *__restrict__ rscale) {
+__device__ void q_split_row(int row, int R, const __nv_bfloat16 *__restrict__ q, uint8_t *__restrict__ qhl,
+                            float *__restrict__ rscale) {
     const int lane = threadIdx.x & 31;
-    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (row >= R) return;
     const __nv_bfloat16 *src = q + (long long)row * kKDim;
     float v[18];
 #pragma unroll
@@ -338,6 +336,8 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_dep_wait();  // the plan (and the FP8 Q split) of this call
+    grid_dep_launch();
     const uint32_t tmem = ctl->tmem_base;
     const int n_units = p.ctrl[0];
 
@@ -860,15 +860,16 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
 }
 
 // ------------------------------------------------------------------------------ plan
-// Per-rank compaction of every request's pages, in three parallel steps over tiles of 1024
-// pages of one request (grid x = tile within the request, grid y = request):
-//   plan_count_kernel   owner counts per tile;
-//   plan_units_kernel   per (rank, request): exclusive scan of the tile counts (tile bases)
-//                       and the total, then the unit list;
-//   plan_scatter_kernel each page to position base + stable in-tile rank among same-owner pages.
+// Per-rank compaction of every request's pages over tiles of 1024 pages of one request, in
+// two launches:
+//   plan_count_kernel  owner counts per tile (extra blocks: the FP8 Q split);
+//   plan_build_kernel  one block per tile: each page to (pages of its owner in the request's
+//                      earlier tiles) + (stable rank among same-owner pages of its tile); the
+//                      last block: per (rank, request) totals, chunks, partial slots and the
+//                      unit list.
 // Rank d's pages of request b end up, in page order, at d * num_pages + req_page_ptr[b] + pos.
 constexpr int kPlanTile = 1024;
-constexpr int kPlanTileThreads = 256;
+constexpr int kPlanThreads = 512;
 
 __device__ __forceinline__ int page_owner_slot(int v, int N, long long slots_per_rank, int &slot) {
     const int d = N <= 1 ? 0 : v % N;
@@ -878,45 +879,90 @@ __device__ __forceinline__ int page_owner_slot(int v, int N, long long slots_per
     return d;
 }
 
-__global__ void __launch_bounds__(kPlanTileThreads)
-plan_count_kernel(int N, long long slots_per_rank, int tiles_per_req, const int64_t *__restrict__ req_page_ptr,
-                  const int32_t *__restrict__ vpages, int32_t *__restrict__ tile_cnt, int32_t *dev_error) {
-    __shared__ int cnt[kMaxDcpAttn];
-    const int b = blockIdx.y, k = blockIdx.x;
-    const long long p0 = req_page_ptr[b] + (long long)k * kPlanTile, p1 = req_page_ptr[b + 1];
-    if (threadIdx.x < kMaxDcpAttn) cnt[threadIdx.x] = 0;
-    __syncthreads();
-    bool bad = false;
-    for (int e = 0; e < kPlanTile / kPlanTileThreads; ++e) {
-        const long long i = p0 + e * kPlanTileThreads + threadIdx.x;
-        if (i < p1) {
-            int slot;
-            const int d = page_owner_slot(vpages[i], N, slots_per_rank, slot);
-            if (d < 0) bad = true;
-            else atomicAdd(&cnt[d], 1);
-        }
+__global__ void __launch_bounds__(kPlanThreads)
+plan_count_kernel(int N, long long slots_per_rank, int tiles_per_req, int tile_stride, int n_tile_blocks,
+                  const int64_t *__restrict__ req_page_ptr, const int32_t *__restrict__ vpages,
+                  int32_t *__restrict__ tile_cnt, int32_t *dev_error, int R, const __nv_bfloat16 *__restrict__ q,
+                  uint8_t *__restrict__ qhl, float *__restrict__ rscale) {
+    grid_dep_wait();
+    grid_dep_launch();
+    if ((int)blockIdx.x >= n_tile_blocks) {  // FP8 Q split: one warp per query row
+        const int row = ((int)blockIdx.x - n_tile_blocks) * (kPlanThreads / 32) + (int)(threadIdx.x >> 5);
+        if (row < R) q_split_row(row, R, q, qhl, rscale);
+        return;
     }
-    __syncthreads();
-    if (p0 < p1 && threadIdx.x < N) tile_cnt[((long long)b * tiles_per_req + k) * kMaxDcpAttn + threadIdx.x] = cnt[threadIdx.x];
+    __shared__ int cnt[kMaxDcpAttn];
+    const int b = blockIdx.x / tile_stride, k0 = blockIdx.x % tile_stride;
+    const long long r0 = req_page_ptr[b], r1 = req_page_ptr[b + 1];
+    bool bad = false;
+    for (int k = k0; r0 + (long long)k * kPlanTile < r1; k += tile_stride) {  // block-uniform
+        const long long p0 = r0 + (long long)k * kPlanTile;
+        if (threadIdx.x < kMaxDcpAttn) cnt[threadIdx.x] = 0;
+        __syncthreads();
+        for (int e = 0; e < kPlanTile / kPlanThreads; ++e) {
+            const long long i = p0 + e * kPlanThreads + threadIdx.x;
+            if (i < r1) {
+                int slot;
+                const int d = page_owner_slot(vpages[i], N, slots_per_rank, slot);
+                if (d < 0) bad = true;
+                else atomicAdd(&cnt[d], 1);
+            }
+        }
+        __syncthreads();
+        if (threadIdx.x < N) tile_cnt[((long long)b * tiles_per_req + k) * kMaxDcpAttn + threadIdx.x] = cnt[threadIdx.x];
+    }
     if (bad && dev_error) atomicOr(dev_error, DCP_DEVERR_OUT_OF_RANGE);
 }
 
-__global__ void __launch_bounds__(kPlanTileThreads)
-plan_scatter_kernel(int N, long long num_pages, long long slots_per_rank, int tiles_per_req,
-                    const int64_t *__restrict__ req_page_ptr, const int32_t *__restrict__ vpages,
-                    const int32_t *__restrict__ tile_base, int32_t *__restrict__ comp_slot,
-                    int32_t *__restrict__ comp_page) {
-    __shared__ int wcnt[kPlanTileThreads / 32][kMaxDcpAttn];
+// Exclusive scan of one value per thread over the block (blockDim.x a multiple of 32).
+__device__ long long block_exclusive_scan(long long x, long long *scratch, long long *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    long long incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const long long t = lane < nw ? scratch[lane] : 0;
+        long long s = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const long long y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        if (lane < nw) scratch[lane] = s - t;
+        if (lane == 31) scratch[32] = s;
+    }
+    __syncthreads();
+    const long long r = scratch[warp] + incl - x;
+    *total = scratch[32];
+    __syncthreads();
+    return r;
+}
+
+// One block per 1024-page tile of a request: stable scatter of its pages.
+__device__ void plan_scatter_tile(int b, int k, int N, long long num_pages, long long slots_per_rank,
+                                  int tiles_per_req, const int64_t *__restrict__ req_page_ptr,
+                                  const int32_t *__restrict__ vpages, const int32_t *__restrict__ tile_cnt,
+                                  int32_t *__restrict__ comp_slot, int32_t *__restrict__ comp_page) {
+    __shared__ int wcnt[kPlanThreads / 32][kMaxDcpAttn];
     __shared__ int run[kMaxDcpAttn];
-    const int b = blockIdx.y, k = blockIdx.x;
     const long long r0 = req_page_ptr[b];
     const long long p0 = r0 + (long long)k * kPlanTile, p1 = req_page_ptr[b + 1];
     if (p0 >= p1) return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    if (threadIdx.x < kMaxDcpAttn)
-        run[threadIdx.x] = threadIdx.x < N ? tile_base[((long long)b * tiles_per_req + k) * kMaxDcpAttn + threadIdx.x] : 0;
-    for (int e = 0; e < kPlanTile / kPlanTileThreads; ++e) {
-        const long long i = p0 + e * kPlanTileThreads + threadIdx.x;
+    __syncthreads();  // the previous tile of this block is done with run[] and wcnt[]
+    if (threadIdx.x < kMaxDcpAttn) {
+        int base = 0;  // pages of this owner in the request's earlier tiles
+        if (threadIdx.x < N)
+            for (int kk = 0; kk < k; ++kk) base += tile_cnt[((long long)b * tiles_per_req + kk) * kMaxDcpAttn + threadIdx.x];
+        run[threadIdx.x] = base;
+    }
+    for (int e = 0; e < kPlanTile / kPlanThreads; ++e) {
+        const long long i = p0 + e * kPlanThreads + threadIdx.x;
         int d = -1, slot = 0;
         if (i < p1) d = page_owner_slot(vpages[i], N, slots_per_rank, slot);
         int my_rank_in_warp = 0;
@@ -936,72 +982,37 @@ plan_scatter_kernel(int N, long long num_pages, long long slots_per_rank, int ti
         __syncthreads();
         if (threadIdx.x < N) {
             int t = 0;
-            for (int w = 0; w < kPlanTileThreads / 32; ++w) t += wcnt[w][threadIdx.x];
+            for (int w = 0; w < kPlanThreads / 32; ++w) t += wcnt[w][threadIdx.x];
             run[threadIdx.x] += t;
         }
         __syncthreads();
     }
 }
 
-// Single block: chunk each (rank, request) pair, assign partial slots, emit units largest
-// first with the G query groups of one chunk adjacent.
-constexpr int kPlanThreads = 1024;
-
-__device__ long long block_exclusive_scan(long long x, long long *scratch, long long *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    long long incl = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) scratch[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const long long t = scratch[lane];
-        long long s = t;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const long long y = __shfl_up_sync(0xffffffffu, s, o);
-            if (lane >= o) s += y;
-        }
-        scratch[lane] = s - t;
-        if (lane == 31) scratch[32] = s;
-    }
-    __syncthreads();
-    const long long r = scratch[warp] + incl - x;
-    *total = scratch[32];
-    __syncthreads();
-    return r;
-}
-
-__global__ void __launch_bounds__(kPlanThreads)
-plan_units_kernel(int B, int N, int G, int only_rank, int tpc, const int64_t *__restrict__ req_page_ptr,
-                  int tiles_per_req, const int32_t *__restrict__ tile_cnt, int32_t *__restrict__ tile_base,
-                  int32_t *__restrict__ counts, int32_t *__restrict__ pair_chunks, int32_t *__restrict__ pair_part,
-                  int4 *__restrict__ units, int *__restrict__ ctrl) {
+// The last block of plan_build_kernel: chunk each (rank, request) pair, assign partial slots,
+// list the multi-chunk pairs, emit units largest first with the G query groups of a chunk
+// adjacent.
+__device__ void plan_build_units(int B, int N, int G, int only_rank, int tpc, const int64_t *__restrict__ req_page_ptr,
+                                 int tiles_per_req, const int32_t *__restrict__ tile_cnt, int32_t *__restrict__ counts,
+                                 int32_t *__restrict__ pair_chunks, int32_t *__restrict__ pair_part,
+                                 int32_t *__restrict__ multi_list, int4 *__restrict__ units, int *__restrict__ ctrl) {
     __shared__ int hist[kMaxTpc + 1];
     __shared__ long long scratch[33];
+    __shared__ int n_multi;
     const int n_pair = N * B;
-    // per (rank, request): exclusive scan of the tile counts and the total
-    for (int pr = threadIdx.x; pr < n_pair; pr += kPlanThreads) {
+    if (threadIdx.x == 0) n_multi = 0;
+    for (int pr = threadIdx.x; pr < n_pair; pr += blockDim.x) {  // per (rank, request) totals
         const int d = pr / B, b = pr % B;
         const long long np = req_page_ptr[b + 1] - req_page_ptr[b];
         const int nt = (int)((np + kPlanTile - 1) / kPlanTile);
         int acc = 0;
-        for (int k = 0; k < nt; ++k) {
-            const long long ix = ((long long)b * tiles_per_req + k) * kMaxDcpAttn + d;
-            const int c = tile_cnt[ix];
-            tile_base[ix] = acc;
-            acc += c;
-        }
+        for (int k = 0; k < nt; ++k) acc += tile_cnt[((long long)b * tiles_per_req + k) * kMaxDcpAttn + d];
         counts[pr] = acc;
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i <= tpc; i += kPlanThreads) hist[i] = 0;
+    for (int i = threadIdx.x; i <= tpc; i += blockDim.x) hist[i] = 0;
     __syncthreads();
     long long running = 0;
-    for (int base = 0; base < n_pair; base += kPlanThreads) {
+    for (int base = 0; base < n_pair; base += blockDim.x) {
         const int pr = base + threadIdx.x;
         int chunks = 0, tiles = 0;
         if (pr < n_pair) {
@@ -1011,6 +1022,7 @@ plan_units_kernel(int B, int N, int G, int only_rank, int tpc, const int64_t *__
                 chunks = tiles == 0 ? 1 : (tiles + tpc - 1) / tpc;
             }
             pair_chunks[pr] = chunks;
+            if (chunks > 1) multi_list[atomicAdd(&n_multi, 1)] = pr;
         }
         long long tot;
         const long long need = chunks > 1 ? (long long)chunks * G : 0;
@@ -1032,9 +1044,10 @@ plan_units_kernel(int B, int N, int G, int only_rank, int tpc, const int64_t *__
         }
         ctrl[0] = acc * G;
         ctrl[1] = 0;
+        ctrl[2] = n_multi;
     }
     __syncthreads();
-    for (int pr = threadIdx.x; pr < n_pair; pr += kPlanThreads) {
+    for (int pr = threadIdx.x; pr < n_pair; pr += blockDim.x) {
         const int chunks = pair_chunks[pr];
         if (chunks == 0) continue;
         const int tiles = (counts[pr] + 1) >> 1;
@@ -1053,28 +1066,53 @@ plan_units_kernel(int B, int N, int G, int only_rank, int tpc, const int64_t *__
     }
 }
 
-// Merge the chunk partials of multi-chunk (rank, request) pairs into O_part / LSE_part.
-__global__ void combine_kernel(int B, int T, int H, int HB, int G, int N, const int32_t *pair_chunks,
-                               const int32_t *pair_part, const float *part_o, const float *part_lse,
+__global__ void __launch_bounds__(kPlanThreads)
+plan_build_kernel(int B, int N, int G, int only_rank, int tpc, long long num_pages, long long slots_per_rank,
+                  int tiles_per_req, int tile_stride, const int64_t *__restrict__ req_page_ptr, const int32_t *__restrict__ vpages,
+                  const int32_t *__restrict__ tile_cnt, int32_t *__restrict__ comp_slot, int32_t *__restrict__ comp_page,
+                  int32_t *__restrict__ counts, int32_t *__restrict__ pair_chunks, int32_t *__restrict__ pair_part,
+                  int32_t *__restrict__ multi_list, int4 *__restrict__ units, int *__restrict__ ctrl) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int n_tile_blocks = B * tile_stride;
+    if ((int)blockIdx.x < n_tile_blocks) {
+        const int b = blockIdx.x / tile_stride;
+        const long long np = req_page_ptr[b + 1] - req_page_ptr[b];
+        for (int k = blockIdx.x % tile_stride; (long long)k * kPlanTile < np; k += tile_stride)
+            plan_scatter_tile(b, k, N, num_pages, slots_per_rank, tiles_per_req, req_page_ptr, vpages, tile_cnt,
+                              comp_slot, comp_page);
+    } else
+        plan_build_units(B, N, G, only_rank, tpc, req_page_ptr, tiles_per_req, tile_cnt, counts, pair_chunks,
+                         pair_part, multi_list, units, ctrl);
+}
+
+// Merge the chunk partials of the multi-chunk (rank, request) pairs listed by the plan into
+// O_part / LSE_part; a grid-stride loop over (listed pair, query group, row), one warp each.
+__global__ void combine_kernel(int B, int T, int H, int HB, int G, const int *__restrict__ ctrl,
+                               const int32_t *__restrict__ multi_list, const int32_t *__restrict__ pair_chunks,
+                               const int32_t *__restrict__ pair_part, const float *part_o, const float *part_lse,
                                float *o_part, float *lse_part) {
-    const long long task = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const long long n_tasks = (long long)N * B * G * kGroupRows;
-    if (task >= n_tasks) return;
-    const int c = (int)(task % kGroupRows);
-    const long long pg = task / kGroupRows;
-    const int g = (int)(pg % G);
-    const int pr = (int)(pg / G);
-    const int chunks = pair_chunks[pr];
-    if (chunks <= 1) return;
-    const int t = g / HB, hb = g % HB;
-    const int rows_valid = min(kGroupRows, H - hb * kGroupRows);
-    if (c >= rows_valid) return;
-    const int d = pr / B, b = pr % B;
-    const long long first = (long long)pair_part[pr] + g;  // chunk k lives at first + k * G
-    const long long out_row = (long long)d * B * T * H + ((long long)(b * T + t) * H) + hb * kGroupRows + c;
-    warp_merge_row512(chunks, part_o + (first * kGroupRows + c) * kVDim, (long long)G * kGroupRows * kVDim,
-                      part_lse + first * kGroupRows + c, (long long)G * kGroupRows,
-                      o_part + out_row * kVDim, lse_part + out_row, 1.f);
+    grid_dep_wait();
+    grid_dep_launch();
+    const long long n_tasks = (long long)ctrl[2] * G * kGroupRows;
+    const int wpb = blockDim.x >> 5;
+    for (long long task = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); task < n_tasks;
+         task += (long long)gridDim.x * wpb) {
+        const int c = (int)(task % kGroupRows);
+        const long long pg = task / kGroupRows;
+        const int g = (int)(pg % G);
+        const int pr = multi_list[pg / G];
+        const int chunks = pair_chunks[pr];
+        const int t = g / HB, hb = g % HB;
+        const int rows_valid = min(kGroupRows, H - hb * kGroupRows);
+        if (c >= rows_valid) continue;
+        const int d = pr / B, b = pr % B;
+        const long long first = (long long)pair_part[pr] + g;  // chunk k lives at first + k * G
+        const long long out_row = (long long)d * B * T * H + ((long long)(b * T + t) * H) + hb * kGroupRows + c;
+        warp_merge_row512(chunks, part_o + (first * kGroupRows + c) * kVDim, (long long)G * kGroupRows * kVDim,
+                          part_lse + first * kGroupRows + c, (long long)G * kGroupRows,
+                          o_part + out_row * kVDim, lse_part + out_row, 1.f);
+    }
 }
 
 // ------------------------------------------------------------------------ tensor maps
@@ -1155,9 +1193,10 @@ bool plan_attention(int B, int T, int H, int N, int64_t num_pages, int dtype, in
     s->off_pages = off;   off = align256(off + sizeof(int32_t) * (size_t)N * num_pages);
     s->off_units = off;   off = align256(off + sizeof(int4) * (size_t)s->max_units);
     s->off_seg = off;     off = align256(off + sizeof(int32_t) * 2 * (size_t)N * B);
+    s->off_multi = off;   off = align256(off + sizeof(int32_t) * (size_t)N * B);
     s->off_ctrl = off;    off = align256(off + sizeof(int32_t) * 4);
     s->tiles_per_req = (int)std::max<long long>(1, (num_pages + kPlanTile - 1) / kPlanTile);
-    s->off_tiles = off;   off = align256(off + sizeof(int32_t) * 2 * (size_t)B * s->tiles_per_req * kMaxDcpAttn);
+    s->off_tiles = off;   off = align256(off + sizeof(int32_t) * (size_t)B * s->tiles_per_req * kMaxDcpAttn);
     s->off_part_o = off;  off = align256(off + sizeof(float) * (size_t)s->max_partials * kGroupRows * kVDim);
     s->off_part_lse = off; off = align256(off + sizeof(float) * (size_t)s->max_partials * kGroupRows);
     const size_t R = (size_t)B * T * H;
@@ -1172,8 +1211,8 @@ int launch_kernel(const AttnMaps &maps, const KParams &kp, int grid, cudaStream_
     constexpr size_t smem = smem_bytes<F8>();
     if (cudaFuncSetAttribute(attn_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return DCP_ERR_CUDA;
-    attn_kernel<F8><<<grid, kThreads, smem, stream>>>(maps, kp);
-    return cudaGetLastError() == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+    return launch_pdl(attn_kernel<F8>, dim3(grid), dim3(kThreads), smem, stream, maps, kp) == cudaSuccess
+               ? DCP_OK : DCP_ERR_CUDA;
 }
 
 int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
@@ -1195,27 +1234,21 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     const int R = s.B * s.T * s.H;
 
     int32_t *tile_cnt = reinterpret_cast<int32_t *>(ws + s.off_tiles);
-    int32_t *tile_base = tile_cnt + (size_t)s.B * s.tiles_per_req * kMaxDcpAttn;
-    const dim3 tgrid((unsigned)s.tiles_per_req, (unsigned)s.B);
-    if (s.num_pages > 0) {
-        plan_count_kernel<<<tgrid, kPlanTileThreads, 0, stream>>>(s.N, a.slots_per_rank, s.tiles_per_req,
-                                                                   a.req_page_ptr, a.dst_vpages, tile_cnt, a.dev_error);
-        if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
-    }
-    plan_units_kernel<<<1, kPlanThreads, 0, stream>>>(s.B, s.N, s.G, a.only_rank, s.tiles_per_chunk, a.req_page_ptr,
-                                                       s.tiles_per_req, tile_cnt, tile_base, counts, pair_chunks,
-                                                       pair_part, units, ctrl);
-    if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
-    if (s.num_pages > 0) {
-        plan_scatter_kernel<<<tgrid, kPlanTileThreads, 0, stream>>>(s.N, s.num_pages, a.slots_per_rank,
-                                                                     s.tiles_per_req, a.req_page_ptr, a.dst_vpages,
-                                                                     tile_base, comp_slot, comp_page);
-        if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
-    }
-    if (f8) {
-        q_split_kernel<<<(R + 7) / 8, 256, 0, stream>>>(R, reinterpret_cast<const __nv_bfloat16 *>(a.q), qhl, qscale);
-        if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
-    }
+    int32_t *multi_list = reinterpret_cast<int32_t *>(ws + s.off_multi);
+    // blocks per request: about three blocks per SM in all, at most one per tile
+    const int tile_stride = (int)std::max<long long>(
+        1, std::min<long long>(s.tiles_per_req, (3LL * num_sms + s.B - 1) / s.B));
+    const int n_tile_blocks = s.B * tile_stride;
+    const int q_blocks = f8 ? (R + kPlanThreads / 32 - 1) / (kPlanThreads / 32) : 0;
+    if (launch_pdl(plan_count_kernel, dim3(n_tile_blocks + q_blocks), dim3(kPlanThreads), 0, stream, s.N,
+                   (long long)a.slots_per_rank, s.tiles_per_req, tile_stride, n_tile_blocks, a.req_page_ptr, a.dst_vpages, tile_cnt,
+                   a.dev_error, R, reinterpret_cast<const __nv_bfloat16 *>(a.q), qhl, qscale) != cudaSuccess)
+        return DCP_ERR_CUDA;
+    if (launch_pdl(plan_build_kernel, dim3(n_tile_blocks + 1), dim3(kPlanThreads), 0, stream, s.B, s.N, s.G,
+                   a.only_rank, s.tiles_per_chunk, (long long)s.num_pages, (long long)a.slots_per_rank, s.tiles_per_req,
+                   tile_stride, a.req_page_ptr, a.dst_vpages, (const int32_t *)tile_cnt, comp_slot, comp_page, counts, pair_chunks,
+                   pair_part, multi_list, units, ctrl) != cudaSuccess)
+        return DCP_ERR_CUDA;
 
     AttnMaps maps;
     memset(&maps, 0, sizeof(maps));
@@ -1261,11 +1294,14 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     const int grid = (int)std::max<long long>(1, std::min<long long>(num_sms, s.max_units));
     const int st = f8 ? launch_kernel<true>(maps, kp, grid, stream) : launch_kernel<false>(maps, kp, grid, stream);
     if (st != DCP_OK) return st;
-    const long long n_tasks = (long long)s.N * s.B * s.G * kGroupRows;
-    const int cw = 8;
-    combine_kernel<<<(unsigned)((n_tasks + cw - 1) / cw), 32 * cw, 0, stream>>>(
-        s.B, s.T, s.H, kp.HB, s.G, s.N, pair_chunks, pair_part, part_o, part_lse, a.o_part, a.lse_part);
-    if (cudaGetLastError() != cudaSuccess) return DCP_ERR_CUDA;
+    // one warp per (listed pair, query group, row) when every pair has several chunks, capped
+    const long long max_tasks = (long long)s.N * s.B * s.G * kGroupRows;
+    const int combine_blocks = (int)std::max<long long>(1, std::min<long long>((max_tasks + 7) / 8, 8LL * num_sms));
+    if (launch_pdl(combine_kernel, dim3(combine_blocks), dim3(256), 0, stream, s.B, s.T, s.H, kp.HB, s.G,
+                   (const int *)ctrl, (const int32_t *)multi_list, (const int32_t *)pair_chunks,
+                   (const int32_t *)pair_part, (const float *)part_o, (const float *)part_lse, a.o_part,
+                   a.lse_part) != cudaSuccess)
+        return DCP_ERR_CUDA;
     return DCP_OK;
 }
 

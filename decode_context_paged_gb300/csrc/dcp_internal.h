@@ -20,6 +20,24 @@ constexpr int kMaxDcpAttn = DCP_MAX_RANKS;
 // Default limit for one device-side pipeline wait (nanoseconds of wall time).
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
+// Launch `kernel` on `stream` with programmatic stream serialization (the kernel calls
+// grid_dep_wait() before touching global memory, so this is safe after any predecessor).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- reshard (dcp_reshard.cu)
 struct ReshardArgs {
     const int64_t *req_page_ptr;
@@ -61,7 +79,7 @@ struct AttnPlanShape {
     int64_t max_partials;
     int64_t n_seg;
     size_t off_counts, off_slots, off_pages, off_units, off_seg, off_ctrl, off_part_o,
-        off_part_lse, off_qhl, off_qscale, off_tiles;
+        off_part_lse, off_qhl, off_qscale, off_tiles, off_multi;
     int tiles_per_req;
     size_t total_bytes;
 };

@@ -17,7 +17,7 @@ __device__ __forceinline__ void warp_merge_row512(int n, const float *o, int64_t
                                                   float *o_out, float *lse_out, float scale) {
     const int lane = threadIdx.x & 31;
     float mx = -INFINITY;
-    for (int i = lane; i < n; i += 32) mx = fmaxf(mx, lse[i * lse_stride]);
+    for (int i = lane; i < n; i += 32) mx = fmaxf(mx, __ldcg(lse + i * lse_stride));
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, s));
     float4 *dst = reinterpret_cast<float4 *>(o_out);
@@ -29,19 +29,32 @@ __device__ __forceinline__ void warp_merge_row512(int n, const float *o, int64_t
     }
     float acc[4][4] = {};
     float wsum = 0.f;
-    for (int i = 0; i < n; ++i) {
-        const float l = lse[i * lse_stride];
-        if (l == -INFINITY) continue;
-        const float w = expf(l - mx);
-        wsum += w;
-        const float4 *src = reinterpret_cast<const float4 *>(o + i * o_stride);
+    for (int i0 = 0; i0 < n; i0 += 4) {  // four partial rows' loads in flight
+        float4 x[4][4];
+        float w[4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float4 x = src[lane + 32 * k];
-            acc[k][0] = fmaf(w, x.x, acc[k][0]);
-            acc[k][1] = fmaf(w, x.y, acc[k][1]);
-            acc[k][2] = fmaf(w, x.z, acc[k][2]);
-            acc[k][3] = fmaf(w, x.w, acc[k][3]);
+        for (int j = 0; j < 4; ++j) {
+            const int i = i0 + j;
+            w[j] = 0.f;
+            if (i < n) {
+                const float l = __ldcg(lse + i * lse_stride);
+                w[j] = (l == -INFINITY) ? 0.f : expf(l - mx);
+                const float4 *src = reinterpret_cast<const float4 *>(o + i * o_stride);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) x[j][k] = __ldcg(src + lane + 32 * k);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (w[j] == 0.f) continue;
+            wsum += w[j];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                acc[k][0] = fmaf(w[j], x[j][k].x, acc[k][0]);
+                acc[k][1] = fmaf(w[j], x[j][k].y, acc[k][1]);
+                acc[k][2] = fmaf(w[j], x[j][k].z, acc[k][2]);
+                acc[k][3] = fmaf(w[j], x[j][k].w, acc[k][3]);
+            }
         }
     }
     const float inv = scale / wsum;

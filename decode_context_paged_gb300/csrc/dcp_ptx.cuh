@@ -14,6 +14,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// ------------------------------------------------------------ programmatic dependent launch
+// Kernels of the library are launched with programmatic stream serialization: a kernel may
+// start while its predecessor in the stream drains.  grid_dep_wait() blocks until every
+// prerequisite grid has completed and its memory is visible (immediately when there is
+// none); each kernel calls it before its first global-memory access.  grid_dep_launch()
+// lets the next kernel in the stream begin launching.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

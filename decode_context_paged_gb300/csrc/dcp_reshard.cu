@@ -30,6 +30,8 @@ __global__ void __launch_bounds__(32, 1) reshard_kernel(const __grid_constant__ 
     extern __shared__ __align__(128) uint8_t smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * kChunk);
     __shared__ int abort_flag;
+    grid_dep_wait();
+    grid_dep_launch();
     if (threadIdx.x != 0) return;
     abort_flag = 0;
     for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
@@ -115,6 +117,8 @@ filter_kernel(int64_t n, const int32_t *__restrict__ dst_vpages,
               int64_t *__restrict__ out_count) {
     __shared__ int warp_tot[kFilterThreads / 32];
     __shared__ int64_t running;
+    grid_dep_wait();
+    grid_dep_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (tid == 0) running = 0;
     __syncthreads();
@@ -172,16 +176,14 @@ cudaError_t launch_reshard(const ReshardArgs &a, int num_sms, cudaStream_t strea
     cudaError_t e = cudaFuncSetAttribute(reshard_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kReshardSmem);
     if (e != cudaSuccess) return e;
-    reshard_kernel<<<num_sms, 32, kReshardSmem, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(reshard_kernel, dim3(num_sms), dim3(32), kReshardSmem, stream, a);
 }
 
 cudaError_t launch_filter(int64_t n, const int32_t *dst_vpages, const int32_t *transfer_idx,
                           int n_dcp, int d, int32_t *out_slot, int32_t *out_src,
                           int64_t *out_count, cudaStream_t stream) {
-    filter_kernel<<<1, kFilterThreads, 0, stream>>>(n, dst_vpages, transfer_idx, n_dcp, d, out_slot,
-                                                     out_src, out_count);
-    return cudaGetLastError();
+    return launch_pdl(filter_kernel, dim3(1), dim3(kFilterThreads), 0, stream, n, dst_vpages, transfer_idx, n_dcp, d,
+                      out_slot, out_src, out_count);
 }
 
 }  // namespace dcp
