@@ -4,6 +4,8 @@ One step = one pass of the whole path over one batch: the page-level reshard fro
 layer-split source layout into the DCP page-interleaved pools, partial MLA decode attention
 on every DCP rank, and the exact LSE merge.  Default workload: 32 requests x 8192 tokens,
 64 heads, q_len 1, BF16 KV, page 64, DCP=8, resharded from one CP source shard (1 layer).
+The attention and the merge run as one library call (dcp_decode_attn_merged); --unfused
+times dcp_partial_decode_attn and dcp_lse_merge as separate calls.
 
 Prints one JSON line.  --impl reference times the float64 CPU oracle instead (bounded
 sample of the same workload, on the host cores).
@@ -130,8 +132,9 @@ class Workload:
     per-step algorithmic bytes.  A step = reshard all layers, then per layer partial attention
     on every DCP rank and the LSE merge."""
 
-    def __init__(self, name: str, device, seed: int = 1):
+    def __init__(self, name: str, device, seed: int = 1, fused: bool = True):
         import decode_context_paged_gb300 as dcp
+        self.fused = fused
         lens_fn, self.H, self.T, self.N, self.dtype, self.L, self.n_cp, slots = WORKLOADS[name]
         lens = lens_fn()
         self.lens = lens
@@ -165,8 +168,11 @@ class Workload:
         self.flops_attn = 2 * keys * self.H * (576 + 512) * self.L
         self.name = (f"{name}-{self.B}x{max(lens)}-h{self.H}-q{self.T}-{self.dtype}-dcp{self.N}"
                      + (f"-L{self.L}-cp{self.n_cp}" if self.L > 1 else ""))
-        # reshard + per layer: plan count (+ FP8 Q split), plan build, attention, combine, merge
+        # reshard + per layer: plan count (+ FP8 Q split), plan build, attention, chunk combine, merge
         self.launches_per_step = 1 + self.L * 5
+        # CUDA-event stages: the fused attention call moves the merge's bytes into its stage
+        self.stage_bytes = ({"reshard": self.bytes["reshard"], "attn": self.bytes["attn"] + self.bytes["merge"]}
+                            if fused else dict(self.bytes))
 
     def step(self, dcp, events=None):
         """events: dict stage -> list of (start, end) event pairs, appended per call."""
@@ -185,6 +191,12 @@ class Workload:
         rec("reshard", lambda: dcp.reshard_pages(rc.req_page_ptr, rc.src_pages, rc.dst_vpages, self.L, rc.src_pools,
                                                  rc.src_pool_pages, rc.dst_pools, rc.dst_slots, dev_error=self.err))
         for l in range(self.L):
+            if self.fused:
+                rec("attn", lambda: dcp.decode_attn_merged(self.q, self.seq_lens, rc.req_page_ptr, rc.dst_vpages,
+                                                           self.layer_pools[l], self.scale, self.kv_scale,
+                                                           o_part=self.o_part, lse_part=self.lse_part, o_out=self.o[l],
+                                                           lse_out=self.lse[l], workspace=self.ws, dev_error=self.err))
+                continue
             rec("attn", lambda: dcp.partial_decode_attn(self.q, self.seq_lens, rc.req_page_ptr, rc.dst_vpages,
                                                         self.layer_pools[l], self.scale, self.kv_scale,
                                                         o_part=self.o_part, lse_part=self.lse_part, workspace=self.ws,
@@ -304,7 +316,7 @@ def run_ours(args):
     dist, rank, world, local = dist_setup()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = Workload(args.config, dev, seed=1 + rank)
+    wl = Workload(args.config, dev, seed=1 + rank, fused=not args.unfused)
     stream = torch.cuda.current_stream()
 
     for _ in range(max(args.warmup, 3)):
@@ -366,7 +378,7 @@ def run_ours(args):
     if rank != 0:
         return
     hbm, bf16, bf16_sus, peak_kind = peaks()
-    stage_gbs = {k: wl.bytes[k] / (stage_ms[k] * 1e-3) / 1e9 for k in stage_ms}
+    stage_gbs = {k: wl.stage_bytes[k] / (stage_ms[k] * 1e-3) / 1e9 for k in stage_ms}
     attn_tflops = wl.flops_attn / (stage_ms["attn"] * 1e-3) / 1e12
     dom = max(stage_ms, key=stage_ms.get)
     kernel_of = {"reshard": "reshard_kernel", "attn": "attn_kernel", "merge": "lse_merge_kernel"}
@@ -375,7 +387,7 @@ def run_ours(args):
     traffic = tr[1] if tr and tr[0] == _src_hash(src_of[dom]) else None
     # the tensor roofline uses the peak of the MMA kind executed (kind::f8f6f4 = 2x the BF16 rate)
     tc_peak = bf16 * (2.0 if wl.dtype == "e4m3" else 1.0)
-    attn_bound = "tensor" if wl.flops_attn / tc_peak / 1e12 > wl.bytes["attn"] / hbm / 1e9 else "hbm"
+    attn_bound = "tensor" if wl.flops_attn / tc_peak / 1e12 > wl.stage_bytes["attn"] / hbm / 1e9 else "hbm"
     if dom == "attn" and attn_bound == "tensor":
         roof = {"kernel": "attn_kernel", "bound": "tensor", "achieved": attn_tflops, "peak": tc_peak,
                 "unit": "TFLOP/s", "frac": attn_tflops / tc_peak, "peak_kind": peak_kind + (
@@ -384,7 +396,7 @@ def run_ours(args):
     else:
         roof = {"kernel": kernel_of[dom], "bound": "hbm", "achieved": stage_gbs[dom], "peak": hbm, "unit": "GB/s",
                 "frac": stage_gbs[dom] / hbm, "peak_kind": peak_kind, "traffic": traffic,
-                "algorithmic_bytes": wl.bytes[dom]}
+                "algorithmic_bytes": wl.stage_bytes[dom]}
     cpu = None
     if not args.no_cpu_baseline:
         gbs, desc, secs, threads = oracle_sample(wl, max_seconds=args.ref_seconds)
@@ -399,11 +411,13 @@ def run_ours(args):
         "stages": {
             "reshard": {"ms": stage_ms["reshard"], "GB/s": stage_gbs["reshard"], "frac_hbm": stage_gbs["reshard"] / hbm},
             "attn": {"ms": stage_ms["attn"], "GB/s": stage_gbs["attn"], "TFLOP/s": attn_tflops,
-                     "frac_hbm": stage_gbs["attn"] / hbm, "frac_tensor": attn_tflops / tc_peak, "bound": attn_bound},
-            "merge": {"ms": stage_ms["merge"], "GB/s": stage_gbs["merge"], "frac_hbm": stage_gbs["merge"] / hbm},
+                     "frac_hbm": stage_gbs["attn"] / hbm, "frac_tensor": attn_tflops / tc_peak, "bound": attn_bound,
+                     "includes_merge": wl.fused},
+            **({} if wl.fused else {"merge": {"ms": stage_ms["merge"], "GB/s": stage_gbs["merge"],
+                                              "frac_hbm": stage_gbs["merge"] / hbm}}),
             "attn_plus_merge_frac_of_roofline": (
                 max((wl.bytes["attn"] + wl.bytes["merge"]) / hbm / 1e9, wl.flops_attn / tc_peak / 1e12)
-                / ((stage_ms["attn"] + stage_ms["merge"]) * 1e-3)),
+                / ((stage_ms["attn"] + stage_ms.get("merge", 0.0)) * 1e-3)),
         },
         "roofline": roof,
         "cpu_baseline": cpu,
@@ -424,6 +438,8 @@ def main():
     ap.add_argument("--config", choices=sorted(WORKLOADS), default="batch")
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--unfused", action="store_true",
+                    help="partial attention and the LSE merge as separate calls (default: one call)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -68,6 +68,9 @@ def _load():
         lib.dcp_partial_decode_attn_static.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, f32,
                                                        i32, vp, i64, i32, vp, vp, vp, vp]
         lib.dcp_partial_decode_attn_static.restype = i32
+        lib.dcp_decode_attn_merged.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, f32, i32, vp,
+                                               i64, vp, vp, vp, vp, vp, sz, vp, vp]
+        lib.dcp_decode_attn_merged.restype = i32
         lib.dcp_lse_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp, vp]
         lib.dcp_lse_merge.restype = i32
         _lib = lib
@@ -216,6 +219,50 @@ def partial_decode_attn(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: t
                                            _dptr(dev_error, "dev_error", torch.int32), _stream(stream)),
            "dcp_partial_decode_attn")
     return o_part, lse_part
+
+
+def decode_attn_merged(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: torch.Tensor,
+                       dst_vpages: torch.Tensor, kv_pools: list, softmax_scale: float, kv_scale: float = 1.0,
+                       o_part: torch.Tensor | None = None, lse_part: torch.Tensor | None = None,
+                       o_out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, dev_error: torch.Tensor | None = None, stream=None):
+    """Every rank's partial attention plus their exact LSE merge in one call.
+    Returns (o_out [B][T][H][512], lse_out [B][T][H], o_part, lse_part), all fp32."""
+    B, T, H, kd = q.shape
+    if kd != K_DIM:
+        raise ValueError("q must be [B][T][H][576]")
+    N = len(kv_pools)
+    slots = kv_pools[0].shape[0]
+    dtype = _kv_code(kv_pools[0])
+    for p in kv_pools:
+        if p.shape != (slots, PAGE, K_DIM) or p.dtype != kv_pools[0].dtype:
+            raise ValueError("every kv pool must be [slots][64][576] of one dtype")
+    dev = q.device
+    if o_part is None:
+        o_part = torch.empty((N, B, T, H, V_DIM), dtype=torch.float32, device=dev)
+    if lse_part is None:
+        lse_part = torch.empty((N, B, T, H), dtype=torch.float32, device=dev)
+    if o_out is None:
+        o_out = torch.empty((B, T, H, V_DIM), dtype=torch.float32, device=dev)
+    if lse_out is None:
+        lse_out = torch.empty((B, T, H), dtype=torch.float32, device=dev)
+    num_pages = dst_vpages.numel()
+    if workspace is None:
+        workspace = alloc_workspace(B, T, H, N, num_pages, dev)
+    kp = _ptr_array(kv_pools, "kv_pools")
+    _check(_load().dcp_decode_attn_merged(B, T, H, _dptr(q, "q", torch.bfloat16),
+                                          _dptr(seq_lens, "seq_lens", torch.int32),
+                                          _dptr(req_page_ptr, "req_page_ptr", torch.int64), num_pages,
+                                          _dptr(dst_vpages, "dst_vpages", torch.int32), PAGE, dtype,
+                                          float(kv_scale), float(softmax_scale), N, ctypes.addressof(kp), slots,
+                                          _dptr(o_part, "o_part", torch.float32),
+                                          _dptr(lse_part, "lse_part", torch.float32),
+                                          _dptr(o_out, "o_out", torch.float32),
+                                          _dptr(lse_out, "lse_out", torch.float32),
+                                          _dptr(workspace, "workspace"), workspace.numel(),
+                                          _dptr(dev_error, "dev_error", torch.int32), _stream(stream)),
+           "dcp_decode_attn_merged")
+    return o_out, lse_out, o_part, lse_part
 
 
 def partial_decode_attn_static(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: torch.Tensor,

@@ -146,12 +146,12 @@ size_t dcp_partial_decode_attn_workspace_size(int num_requests, int q_len, int n
     return s.total_bytes > s8.total_bytes ? s.total_bytes : s8.total_bytes;
 }
 
-int dcp_partial_decode_attn(int num_requests, int q_len, int num_heads, const void *q,
+static int partial_attn_impl(int num_requests, int q_len, int num_heads, const void *q,
                             const int32_t *seq_lens, const int64_t *req_page_ptr,
                             int64_t num_pages, const int32_t *dst_vpages, int page_size,
                             int dtype, float kv_scale, float softmax_scale, int n_dcp,
                             const void *const *kv_pools, int64_t slots_per_rank, int only_rank,
-                            float *o_part, float *lse_part, void *workspace,
+                            float *o_part, float *lse_part, float *o_out, float *lse_out, void *workspace,
                             size_t workspace_bytes, int32_t *dev_error, dcp_stream_t stream) {
     if (num_requests < 0 || q_len < 1 || num_heads < 1 || num_pages < 0 || page_size != kPage)
         return DCP_ERR_INVALID_ARG;
@@ -184,10 +184,37 @@ int dcp_partial_decode_attn(int num_requests, int q_len, int num_heads, const vo
     a.only_rank = only_rank;
     a.o_part = o_part;
     a.lse_part = lse_part;
+    a.o_out = o_out;
+    a.lse_out = lse_out;
     a.workspace = static_cast<uint8_t *>(workspace);
     a.dev_error = dev_error;
     a.wait_limit_ns = wait_limit_ns();
     return launch_attention(a, sms, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dcp_partial_decode_attn(int num_requests, int q_len, int num_heads, const void *q,
+                            const int32_t *seq_lens, const int64_t *req_page_ptr,
+                            int64_t num_pages, const int32_t *dst_vpages, int page_size,
+                            int dtype, float kv_scale, float softmax_scale, int n_dcp,
+                            const void *const *kv_pools, int64_t slots_per_rank, int only_rank,
+                            float *o_part, float *lse_part, void *workspace,
+                            size_t workspace_bytes, int32_t *dev_error, dcp_stream_t stream) {
+    return partial_attn_impl(num_requests, q_len, num_heads, q, seq_lens, req_page_ptr, num_pages, dst_vpages,
+                             page_size, dtype, kv_scale, softmax_scale, n_dcp, kv_pools, slots_per_rank, only_rank,
+                             o_part, lse_part, nullptr, nullptr, workspace, workspace_bytes, dev_error, stream);
+}
+
+int dcp_decode_attn_merged(int num_requests, int q_len, int num_heads, const void *q,
+                           const int32_t *seq_lens, const int64_t *req_page_ptr, int64_t num_pages,
+                           const int32_t *dst_vpages, int page_size, int dtype, float kv_scale,
+                           float softmax_scale, int n_dcp, const void *const *kv_pools,
+                           int64_t slots_per_rank, float *o_part, float *lse_part, float *o_out,
+                           float *lse_out, void *workspace, size_t workspace_bytes,
+                           int32_t *dev_error, dcp_stream_t stream) {
+    if (num_requests > 0 && (!o_out || !lse_out || !aligned(o_out, 16))) return DCP_ERR_INVALID_ARG;
+    return partial_attn_impl(num_requests, q_len, num_heads, q, seq_lens, req_page_ptr, num_pages, dst_vpages,
+                             page_size, dtype, kv_scale, softmax_scale, n_dcp, kv_pools, slots_per_rank, -1, o_part,
+                             lse_part, o_out, lse_out, workspace, workspace_bytes, dev_error, stream);
 }
 
 int dcp_lse_merge(int n_parts, int64_t rows, int v_dim, const float *o_part, const float *lse_part,

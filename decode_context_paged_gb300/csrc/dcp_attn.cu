@@ -68,12 +68,25 @@ constexpr float kPScale = 4.f;           // FP8 P is stored as 4 * p (p <= 2^6 u
 // this long stays far below the output tolerance, while short segments keep the lo term.
 constexpr int kSinglePMinPages = 128;
 
+#ifndef DCP_ATTN_K_SLOTS_BF16
+#define DCP_ATTN_K_SLOTS_BF16 4
+#endif
+#ifndef DCP_ATTN_P_BUFS_BF16
+#define DCP_ATTN_P_BUFS_BF16 1
+#endif
+#ifndef DCP_ATTN_K_SLOTS_F8
+#define DCP_ATTN_K_SLOTS_F8 4
+#endif
+#ifndef DCP_ATTN_P_BUFS_F8
+#define DCP_ATTN_P_BUFS_F8 1
+#endif
+
 template <bool F8>
 struct Cfg {
     // Four K slots and one P buffer (measured: trading a K slot for a second P buffer is
     // slower for both element types).
-    static constexpr int kKSlots = 4;
-    static constexpr int kPBufs = 1;
+    static constexpr int kKSlots = F8 ? DCP_ATTN_K_SLOTS_F8 : DCP_ATTN_K_SLOTS_BF16;
+    static constexpr int kPBufs = F8 ? DCP_ATTN_P_BUFS_F8 : DCP_ATTN_P_BUFS_BF16;
     static constexpr uint32_t kOffV = kKSlots * kKSlotBytes;
     static constexpr uint32_t kOffQ = kOffV + kVSlots * kVSlotBytes;
     static constexpr uint32_t kOffP = kOffQ + kQBytes;
@@ -100,11 +113,11 @@ struct __align__(16) Ctl {
     float corr[64];
     float oscale[64];
     float qscale[64];            // per query row: softmax_scale * kappa * log2(e) * 2^-qexp
-    uint64_t kfull[4], kempty[4];
+    uint64_t kfull[8], kempty[8];
     uint64_t vfull[kVSlots], vempty[kVSlots];
     uint64_t q_full, q_empty;
     uint64_t s_full[3], s_free[3];
-    uint64_t p_full, o_done[2], o_free;
+    uint64_t p_full[2], o_done[2], o_free;  // p_full[t & 1]: P of global tile t written
     uint64_t unit_full[2], unit_empty[2];
     uint64_t drain_s, drain_pv;
     UnitInfo unit[2];
@@ -319,7 +332,8 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
             mbar_init(&ctl->unit_full[i], 1);
             mbar_init(&ctl->unit_empty[i], 7);
         }
-        mbar_init(&ctl->p_full, 512);
+        mbar_init(&ctl->p_full[0], 512);
+        mbar_init(&ctl->p_full[1], 512);
         mbar_init(&ctl->o_done[0], 1);
         mbar_init(&ctl->o_done[1], 1);
         mbar_init(&ctl->o_free, 512);
@@ -556,7 +570,7 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                 const int nt = (u.n_pages + 1) >> 1;
                 if (nt == 0) continue;
                 for (int i = 0; i < nt && ok; ++i) {
-                    if (!mbar_wait(&ctl->p_full, p_cnt & 1, abort_flag, p.dev_error, lim)) {
+                    if (!mbar_wait(&ctl->p_full[p_cnt & 1], (p_cnt >> 1) & 1, abort_flag, p.dev_error, lim)) {
                         ok = false;
                         break;
                     }
@@ -763,7 +777,10 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                         tmem_wait_st();
                     }
                 }
-                if (g >= (uint32_t)C::kPBufs) {  // P buffer g % kPBufs: its previous reader must be done
+                // P buffer g % kPBufs: its previous reader must be done.  (Measured: letting
+                // FP8 single-term tiles alternate between the two 8 KB halves of the buffer is
+                // slower; the P*V bursts then delay the score MMAs that free K slots.)
+                if (g >= (uint32_t)C::kPBufs) {
                     fail = !wait_pv(g - C::kPBufs);
                     if (fail) continue;
                     tc_fence_after();
@@ -813,7 +830,7 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&ctl->p_full);
+                mbar_arrive(&ctl->p_full[g & 1]);
             }
             if (aborted) break;
             fail = !wait_pv(s_cnt - 1);
@@ -1060,7 +1077,8 @@ __device__ void plan_build_units(int B, int N, int G, int only_rank, int tpc, co
             for (int g = 0; g < G; ++g) {
                 const int out = chunks > 1 ? pair_part[pr] + c * G + g : -1;
                 units[(long long)slot * G + g] =
-                    make_int4(pr * G + g, page_begin, n_pages | (cnt >= kSinglePMinPages ? (1 << 30) : 0), out);
+                    make_int4(pr * G + g, page_begin,
+                              n_pages | (cnt >= kSinglePMinPages ? (1 << 30) : 0), out);
             }
         }
     }
@@ -1113,6 +1131,56 @@ __global__ void combine_kernel(int B, int T, int H, int HB, int G, const int *__
                           part_lse + first * kGroupRows + c, (long long)G * kGroupRows,
                           o_part + out_row * kVDim, lse_part + out_row, 1.f);
     }
+}
+
+// Fused merge, first launch after the attention kernel.  With no multi-chunk pair (ctrl[2] ==
+// 0) it merges every row over the ranks, one warp per row, ascending rank order.  Otherwise it combines the chunk partials as combine_kernel does
+// and leaves the rank merge to merge_after_combine_kernel.
+__global__ void merge_combine_kernel(int B, int T, int H, int HB, int G, int N, const int *__restrict__ ctrl,
+                                     const int32_t *__restrict__ multi_list, const int32_t *__restrict__ pair_chunks,
+                                     const int32_t *__restrict__ pair_part, const float *part_o,
+                                     const float *part_lse, float *o_part, float *lse_part, float *o_out,
+                                     float *lse_out) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int n_multi = ctrl[2];
+    const int wpb = blockDim.x >> 5;
+    if (n_multi > 0) {
+        const long long n_tasks = (long long)n_multi * G * kGroupRows;
+        for (long long task = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); task < n_tasks;
+             task += (long long)gridDim.x * wpb) {
+            const int c = (int)(task % kGroupRows);
+            const long long pg = task / kGroupRows;
+            const int g = (int)(pg % G);
+            const int pr = multi_list[pg / G];
+            const int t = g / HB, hb = g % HB;
+            if (c >= min(kGroupRows, H - hb * kGroupRows)) continue;
+            const int d = pr / B, b = pr % B;
+            const long long first = (long long)pair_part[pr] + g;
+            const long long out_row = (long long)d * B * T * H + ((long long)(b * T + t) * H) + hb * kGroupRows + c;
+            warp_merge_row512(pair_chunks[pr], part_o + (first * kGroupRows + c) * kVDim,
+                              (long long)G * kGroupRows * kVDim, part_lse + first * kGroupRows + c,
+                              (long long)G * kGroupRows, o_part + out_row * kVDim, lse_part + out_row, 1.f);
+        }
+        return;
+    }
+    const long long rows = (long long)B * T * H;
+    for (long long row = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * wpb)
+        warp_merge_row512(N, o_part + row * kVDim, rows * kVDim, lse_part + row, rows, o_out + row * kVDim,
+                          lse_out + row, 1.f);
+}
+
+// Fused merge, second launch: the rank merge of every row when merge_combine_kernel combined
+// chunk partials instead (ctrl[2] > 0); exits at once otherwise.
+__global__ void merge_after_combine_kernel(int N, long long rows, const int *__restrict__ ctrl, const float *o_part,
+                                           const float *lse_part, float *o_out, float *lse_out) {
+    grid_dep_wait();
+    grid_dep_launch();
+    if (ctrl[2] == 0) return;
+    const int wpb = blockDim.x >> 5;
+    for (long long row = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * wpb)
+        warp_merge_row512(N, o_part + row * kVDim, rows * kVDim, lse_part + row, rows, o_out + row * kVDim,
+                          lse_out + row, 1.f);
 }
 
 // ------------------------------------------------------------------------ tensor maps
@@ -1235,6 +1303,7 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
 
     int32_t *tile_cnt = reinterpret_cast<int32_t *>(ws + s.off_tiles);
     int32_t *multi_list = reinterpret_cast<int32_t *>(ws + s.off_multi);
+    const bool fused = a.o_out != nullptr;
     // blocks per request: about three blocks per SM in all, at most one per tile
     const int tile_stride = (int)std::max<long long>(
         1, std::min<long long>(s.tiles_per_req, (3LL * num_sms + s.B - 1) / s.B));
@@ -1294,6 +1363,22 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     const int grid = (int)std::max<long long>(1, std::min<long long>(num_sms, s.max_units));
     const int st = f8 ? launch_kernel<true>(maps, kp, grid, stream) : launch_kernel<false>(maps, kp, grid, stream);
     if (st != DCP_OK) return st;
+    if (a.o_out) {  // fused merge (see merge_combine_kernel)
+        const long long rows = (long long)s.B * s.T * s.H;
+        const long long tasks = std::max<long long>(rows, (long long)s.N * s.B * s.G * kGroupRows);
+        const int blocks = (int)std::max<long long>(1, std::min<long long>((tasks + 7) / 8, 8LL * num_sms));
+        if (launch_pdl(merge_combine_kernel, dim3(blocks), dim3(256), 0, stream, s.B, s.T, s.H, kp.HB, s.G, s.N,
+                       (const int *)ctrl, (const int32_t *)multi_list, (const int32_t *)pair_chunks,
+                       (const int32_t *)pair_part, (const float *)part_o, (const float *)part_lse, a.o_part,
+                       a.lse_part, a.o_out, a.lse_out) != cudaSuccess)
+            return DCP_ERR_CUDA;
+        const int mblocks = (int)std::max<long long>(1, std::min<long long>((rows + 7) / 8, 8LL * num_sms));
+        if (launch_pdl(merge_after_combine_kernel, dim3(mblocks), dim3(256), 0, stream, s.N, rows,
+                       (const int *)ctrl, (const float *)a.o_part, (const float *)a.lse_part, a.o_out,
+                       a.lse_out) != cudaSuccess)
+            return DCP_ERR_CUDA;
+        return DCP_OK;
+    }
     // one warp per (listed pair, query group, row) when every pair has several chunks, capped
     const long long max_tasks = (long long)s.N * s.B * s.G * kGroupRows;
     const int combine_blocks = (int)std::max<long long>(1, std::min<long long>((max_tasks + 7) / 8, 8LL * num_sms));

@@ -100,6 +100,8 @@ struct AttnArgs {
     int only_rank;
     float *o_part;
     float *lse_part;
+    float *o_out;    // non-null: also merge the ranks' partials (exact LSE merge) into o_out / lse_out
+    float *lse_out;
     uint8_t *workspace;
     int32_t *dev_error;
     uint64_t wait_limit_ns;

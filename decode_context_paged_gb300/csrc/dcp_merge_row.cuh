@@ -11,7 +11,9 @@
 namespace dcp {
 
 // Partial i's row starts at o + i * o_stride (floats) and its LSE at lse[i * lse_stride].
-// Lane owns float4 columns lane + 32k, k < 4.  `scale` multiplies the merged O.
+// Lane owns float4 columns lane + 32k, k < 4.  `scale` multiplies the merged O.  kPar partial
+// rows have their loads in flight together.
+template <int kPar = 4>
 __device__ __forceinline__ void warp_merge_row512(int n, const float *o, int64_t o_stride,
                                                   const float *lse, int64_t lse_stride,
                                                   float *o_out, float *lse_out, float scale) {
@@ -29,11 +31,11 @@ __device__ __forceinline__ void warp_merge_row512(int n, const float *o, int64_t
     }
     float acc[4][4] = {};
     float wsum = 0.f;
-    for (int i0 = 0; i0 < n; i0 += 4) {  // four partial rows' loads in flight
-        float4 x[4][4];
-        float w[4];
+    for (int i0 = 0; i0 < n; i0 += kPar) {
+        float4 x[kPar][4];
+        float w[kPar];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kPar; ++j) {
             const int i = i0 + j;
             w[j] = 0.f;
             if (i < n) {
@@ -45,7 +47,7 @@ __device__ __forceinline__ void warp_merge_row512(int n, const float *o, int64_t
             }
         }
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < kPar; ++j) {
             if (w[j] == 0.f) continue;
             wsum += w[j];
 #pragma unroll

@@ -172,6 +172,32 @@ int dcp_partial_decode_attn(int num_requests, int q_len, int num_heads, const vo
                             size_t workspace_bytes, int32_t *dev_error, dcp_stream_t stream);
 
 /*
+ * [P1] 5.2 "DCP Attention" followed by "All-Gather + LSE Merge", [P2] (exact recombination),
+ * in one call on one GPU: every rank's partial attention exactly as dcp_partial_decode_attn
+ * with only_rank = -1 (o_part / lse_part are written and hold each rank's result on return),
+ * and the merge of the n_dcp partials of every row exactly as dcp_lse_merge (ascending rank
+ * order; all-empty rows give O = 0, LSE = -inf):
+ *   o_out   fp32 [num_requests][q_len][num_heads][512]
+ *   lse_out fp32 [num_requests][q_len][num_heads]
+ * The merge runs in the launches that follow the attention kernel, while the partials are
+ * still in L2: when no (rank, request) segment was split into chunks, the launch that would
+ * combine chunk partials merges the ranks instead and the last launch exits at once; else the
+ * chunks are combined first and the last launch merges.  The pages' deployment has one GPU
+ * per rank and an all-gather before the merge; on one GPU the gather is a read of the other
+ * ranks' partials.
+ *   workspace: >= dcp_partial_decode_attn_workspace_size(...) bytes, 256-byte aligned.
+ * Returns the statuses of dcp_partial_decode_attn (o_out / lse_out null or o_out not 16-byte
+ * aligned: DCP_ERR_INVALID_ARG).
+ */
+int dcp_decode_attn_merged(int num_requests, int q_len, int num_heads, const void *q,
+                           const int32_t *seq_lens, const int64_t *req_page_ptr, int64_t num_pages,
+                           const int32_t *dst_vpages, int page_size, int dtype, float kv_scale,
+                           float softmax_scale, int n_dcp, const void *const *kv_pools,
+                           int64_t slots_per_rank, float *o_part, float *lse_part, float *o_out,
+                           float *lse_out, void *workspace, size_t workspace_bytes,
+                           int32_t *dev_error, dcp_stream_t stream);
+
+/*
  * Partial attention for callers that cannot allocate device memory.  The pages have no
  * counterpart to this entry point; it exists for callers that cannot call cudaMalloc, such
  * as a host whose pool allocator owns all device memory and hands plug-ins only tensor
