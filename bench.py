@@ -132,9 +132,10 @@ class Workload:
     per-step algorithmic bytes.  A step = reshard all layers, then per layer partial attention
     on every DCP rank and the LSE merge."""
 
-    def __init__(self, name: str, device, seed: int = 1, fused: bool = True):
+    def __init__(self, name: str, device, seed: int = 1, fused: bool = True, staging_mb: int = 0):
         import decode_context_paged_gb300 as dcp
         self.fused = fused
+        self.pack = staging_mb > 0  # reshard stage in bounded pack mode (per path: filter, pack, unpack)
         lens_fn, self.H, self.T, self.N, self.dtype, self.L, self.n_cp, slots = WORKLOADS[name]
         lens = lens_fn()
         self.lens = lens
@@ -170,6 +171,23 @@ class Workload:
                      + (f"-L{self.L}-cp{self.n_cp}" if self.L > 1 else ""))
         # reshard + per layer: plan count (+ FP8 Q split), plan build, attention, chunk combine, merge
         self.launches_per_step = 1 + self.L * 5
+        if self.pack:
+            # per path (r, d): its filtered page count (fixed by the page table, known to the host as in
+            # the pages' sender) and the chunk item ranges through the bounded staging buffer
+            self.staging = torch.empty(staging_mb << 20, dtype=torch.uint8, device=device)
+            vp = self.rc.dst_vpages.cpu()
+            owner = vp % self.N if self.N > 1 else torch.zeros_like(vp)
+            self.pack_paths = []
+            start = 0
+            for r, cnt in enumerate(counts):
+                for d in range(self.N):
+                    n_idx = int((owner == d).sum())
+                    self.pack_paths.append((r, d, start, cnt, n_idx,
+                                            dcp.pack_chunks(cnt * n_idx, self.rc.page_bytes, self.staging.numel())))
+                start += cnt
+            n_chunks = sum(len(p[5]) for p in self.pack_paths)
+            self.launches_per_step += len(self.pack_paths) + 2 * n_chunks - 1
+            self.pack_moved_bytes = 2 * self.bytes["reshard"]  # every page in and out of the staging buffer
         # CUDA-event stages: the fused attention call moves the merge's bytes into its stage
         self.stage_bytes = ({"reshard": self.bytes["reshard"], "attn": self.bytes["attn"] + self.bytes["merge"]}
                             if fused else dict(self.bytes))
@@ -188,8 +206,20 @@ class Workload:
             b.record()
             events.setdefault(stage, []).append((a, b))
 
-        rec("reshard", lambda: dcp.reshard_pages(rc.req_page_ptr, rc.src_pages, rc.dst_vpages, self.L, rc.src_pools,
-                                                 rc.src_pool_pages, rc.dst_pools, rc.dst_slots, dev_error=self.err))
+        def pack_reshard():
+            for r, d, start, cnt, n_idx, chunks in self.pack_paths:
+                slot, src, _ = dcp.filter_page_indices(rc.dst_vpages, self.N, d, rc.src_pages)
+                for begin, n in chunks:
+                    dcp.pack_pages(src, n_idx, cnt, begin, n, rc.src_pools[r], self.staging, dev_error=self.err)
+                    dcp.unpack_pages(slot, n_idx, cnt, start, begin, n, self.staging, rc.dst_pools[d],
+                                     dev_error=self.err)
+
+        if self.pack:
+            rec("reshard", pack_reshard)
+        else:
+            rec("reshard", lambda: dcp.reshard_pages(rc.req_page_ptr, rc.src_pages, rc.dst_vpages, self.L,
+                                                     rc.src_pools, rc.src_pool_pages, rc.dst_pools, rc.dst_slots,
+                                                     dev_error=self.err))
         for l in range(self.L):
             if self.fused:
                 rec("attn", lambda: dcp.decode_attn_merged(self.q, self.seq_lens, rc.req_page_ptr, rc.dst_vpages,
@@ -316,7 +346,7 @@ def run_ours(args):
     dist, rank, world, local = dist_setup()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = Workload(args.config, dev, seed=1 + rank, fused=not args.unfused)
+    wl = Workload(args.config, dev, seed=1 + rank, fused=not args.unfused, staging_mb=args.staging_mb)
     stream = torch.cuda.current_stream()
 
     for _ in range(max(args.warmup, 3)):
@@ -409,7 +439,11 @@ def run_ours(args):
         "config": {"workload": wl.name, "l2": "inputs larger than L2", "bytes_per_step": step_bytes,
                    "parallelism": f"replicas x{world}"},
         "stages": {
-            "reshard": {"ms": stage_ms["reshard"], "GB/s": stage_gbs["reshard"], "frac_hbm": stage_gbs["reshard"] / hbm},
+            "reshard": {"ms": stage_ms["reshard"], "GB/s": stage_gbs["reshard"], "frac_hbm": stage_gbs["reshard"] / hbm,
+                        **({"mode": f"bounded pack, {args.staging_mb} MB staging buffer",
+                            "moved_GB/s": wl.pack_moved_bytes / (stage_ms["reshard"] * 1e-3) / 1e9,
+                            "moved_frac_hbm": wl.pack_moved_bytes / (stage_ms["reshard"] * 1e-3) / 1e9 / hbm}
+                           if wl.pack else {"mode": "direct"})},
             "attn": {"ms": stage_ms["attn"], "GB/s": stage_gbs["attn"], "TFLOP/s": attn_tflops,
                      "frac_hbm": stage_gbs["attn"] / hbm, "frac_tensor": attn_tflops / tc_peak, "bound": attn_bound,
                      "includes_merge": wl.fused},
@@ -438,6 +472,8 @@ def main():
     ap.add_argument("--config", choices=sorted(WORKLOADS), default="batch")
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--staging-mb", type=int, default=0,
+                    help="reshard in bounded pack mode through a staging buffer of this many MB (0: direct)")
     ap.add_argument("--unfused", action="store_true",
                     help="partial attention and the LSE merge as separate calls (default: one call)")
     args = ap.parse_args()

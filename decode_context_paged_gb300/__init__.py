@@ -56,6 +56,10 @@ def _load():
         lib.dcp_layer_range.argtypes = [i32, i32, i32, vp, vp]
         lib.dcp_layer_range.restype = i32
         lib.dcp_filter_page_indices.argtypes = [i64, vp, vp, i32, i32, vp, vp, vp, vp]
+        lib.dcp_pack_pages.argtypes = [i64, vp, i32, i64, i64, i32, vp, i64, vp, sz, vp, vp]
+        lib.dcp_pack_pages.restype = i32
+        lib.dcp_unpack_pages.argtypes = [i64, vp, i32, i32, i64, i64, i32, vp, sz, vp, i32, i64, vp, vp]
+        lib.dcp_unpack_pages.restype = i32
         lib.dcp_filter_page_indices.restype = i32
         lib.dcp_reshard_pages.argtypes = [i32, vp, i64, vp, vp, i32, i32, i32, i32, i32, vp, i64, i32,
                                           vp, i64, i32, i32, vp, vp]
@@ -149,6 +153,42 @@ def filter_page_indices(dst_vpages: torch.Tensor, n_dcp: int, d: int,
                                            _dptr(count, "count"), _stream(stream)),
            "dcp_filter_page_indices")
     return out_slot, out_src, count
+
+
+def pack_chunks(n_items: int, page_bytes: int, staging_bytes: int) -> list:
+    """Item ranges (begin, count) of a path's bounded pack: as many whole pages per chunk as the
+    staging buffer holds; one chunk when everything fits."""
+    per = staging_bytes // page_bytes
+    if per < 1:
+        raise ValueError("the staging buffer holds no page")
+    return [(b, min(per, n_items - b)) for b in range(0, n_items, per)]
+
+
+def pack_pages(src_idx: torch.Tensor, n_idx: int, n_layers: int, item_begin: int, n_items: int,
+               src_pool: torch.Tensor, staging: torch.Tensor, dev_error: torch.Tensor | None = None,
+               stream=None) -> None:
+    """Bounded-pack send side of one path: items [item_begin, item_begin + n_items) (layer-major
+    over the first n_idx entries of src_idx) from src_pool [n_layers][pages][64][576] into staging."""
+    dtype = _kv_code(src_pool)
+    _check(_load().dcp_pack_pages(n_idx, _dptr(src_idx, "src_idx", torch.int32), n_layers, item_begin, n_items,
+                                  dtype, _dptr(src_pool, "src_pool"), src_pool.shape[1], _dptr(staging, "staging"),
+                                  staging.numel() * staging.element_size(), _dptr(dev_error, "dev_error", torch.int32),
+                                  _stream(stream)),
+           "dcp_pack_pages")
+
+
+def unpack_pages(dst_slot: torch.Tensor, n_idx: int, n_layers: int, layer_offset: int, item_begin: int,
+                 n_items: int, staging: torch.Tensor, dst_pool: torch.Tensor, dev_error: torch.Tensor | None = None,
+                 stream=None) -> None:
+    """Bounded-pack receive side: the same items from staging into dst_pool
+    [num_layers][slots][64][576] at layer layer_offset + j, slot dst_slot[i]."""
+    dtype = _kv_code(dst_pool)
+    _check(_load().dcp_unpack_pages(n_idx, _dptr(dst_slot, "dst_slot", torch.int32), n_layers, layer_offset,
+                                    item_begin, n_items, dtype, _dptr(staging, "staging"),
+                                    staging.numel() * staging.element_size(), _dptr(dst_pool, "dst_pool"),
+                                    dst_pool.shape[0], dst_pool.shape[1], _dptr(dev_error, "dev_error", torch.int32),
+                                    _stream(stream)),
+           "dcp_unpack_pages")
 
 
 def reshard_pages(req_page_ptr: torch.Tensor, src_pages: torch.Tensor, dst_vpages: torch.Tensor,

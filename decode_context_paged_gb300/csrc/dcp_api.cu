@@ -135,6 +135,52 @@ int dcp_reshard_pages(int num_requests, const int64_t *req_page_ptr, int64_t num
     return DCP_OK;
 }
 
+static int pack_impl(int64_t n_idx, const int32_t *idx, int n_layers, int layer_offset, int64_t item_begin,
+                     int64_t n_items, int dtype, const void *pool, int64_t pool_pages, int pool_layers,
+                     const void *staging, size_t staging_bytes, int to_staging, int32_t *dev_error,
+                     dcp_stream_t stream) {
+    if (dtype != DCP_KV_BF16 && dtype != DCP_KV_FP8_E4M3) return DCP_ERR_INVALID_ARG;
+    if (n_idx < 0 || n_layers < 0 || item_begin < 0 || n_items < 0 || pool_pages < 0 || pool_layers < 0)
+        return DCP_ERR_INVALID_ARG;
+    if (n_items == 0) return DCP_OK;
+    if (n_idx == 0 || item_begin + n_items > n_idx * (int64_t)n_layers) return DCP_ERR_INVALID_ARG;
+    const int64_t page_bytes = (int64_t)kPage * kKDim * (dtype == DCP_KV_BF16 ? 2 : 1);
+    if (!idx || !pool || !staging || !aligned(pool, 16) || !aligned(staging, 16)) return DCP_ERR_INVALID_ARG;
+    if ((int64_t)staging_bytes < n_items * page_bytes) return DCP_ERR_INVALID_ARG;
+    PackArgs a{};
+    a.idx = idx;
+    a.n_idx = n_idx;
+    a.n_layers = n_layers;
+    a.layer_offset = layer_offset;
+    a.item_begin = item_begin;
+    a.n_items = n_items;
+    a.page_bytes = page_bytes;
+    a.pool = static_cast<uint8_t *>(const_cast<void *>(pool));
+    a.pool_pages = pool_pages;
+    a.pool_layers = pool_layers;
+    a.staging = static_cast<uint8_t *>(const_cast<void *>(staging));
+    a.to_staging = to_staging;
+    a.dev_error = dev_error;
+    a.wait_limit_ns = wait_limit_ns();
+    int sms = 0;
+    if (int st = current_sm_count(&sms)) return st;
+    return launch_pack(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
+int dcp_pack_pages(int64_t n_idx, const int32_t *src_idx, int n_layers, int64_t item_begin, int64_t n_items,
+                   int dtype, const void *src_pool, int64_t src_pool_pages, void *staging, size_t staging_bytes,
+                   int32_t *dev_error, dcp_stream_t stream) {
+    return pack_impl(n_idx, src_idx, n_layers, 0, item_begin, n_items, dtype, src_pool, src_pool_pages, n_layers,
+                     staging, staging_bytes, 1, dev_error, stream);
+}
+
+int dcp_unpack_pages(int64_t n_idx, const int32_t *dst_slot, int n_layers, int layer_offset, int64_t item_begin,
+                     int64_t n_items, int dtype, const void *staging, size_t staging_bytes, void *dst_pool,
+                     int num_layers, int64_t dst_slots, int32_t *dev_error, dcp_stream_t stream) {
+    return pack_impl(n_idx, dst_slot, n_layers, layer_offset, item_begin, n_items, dtype, dst_pool, dst_slots,
+                     num_layers, staging, staging_bytes, 0, dev_error, stream);
+}
+
 size_t dcp_partial_decode_attn_workspace_size(int num_requests, int q_len, int num_heads, int n_dcp,
                                               int64_t num_pages) {
     int sms = 0;

@@ -61,6 +61,24 @@ struct ReshardArgs {
 };
 cudaError_t launch_reshard(const ReshardArgs &a, int num_sms, cudaStream_t stream);
 
+// ---- pack / unpack of one path's pages through a staging buffer (dcp_reshard.cu)
+struct PackArgs {
+    const int32_t *idx;      // [n_idx]: source page indices (pack) or destination slots (unpack)
+    int64_t n_idx;
+    int n_layers;            // layers of the sending rank
+    int layer_offset;        // unpack: destination layer of source layer 0
+    int64_t item_begin, n_items;
+    int64_t page_bytes;
+    uint8_t *pool;           // pack: source pool [n_layers][pool_pages]; unpack: [pool_layers][pool_pages]
+    int64_t pool_pages;
+    int pool_layers;
+    uint8_t *staging;
+    int to_staging;          // 1 = pack, 0 = unpack
+    int32_t *dev_error;
+    uint64_t wait_limit_ns;
+};
+cudaError_t launch_pack(const PackArgs &a, int num_sms, cudaStream_t stream);
+
 cudaError_t launch_filter(int64_t n, const int32_t *dst_vpages, const int32_t *transfer_idx,
                           int n_dcp, int d, int32_t *out_slot, int32_t *out_src,
                           int64_t *out_count, cudaStream_t stream);

@@ -14,53 +14,26 @@
 // chunk ranges of the flattened (layer, page, chunk) space; all (r, d) paths share the launch.
 #include <cuda_runtime.h>
 
+#include "dcp_copy_ring.cuh"
 #include "dcp_internal.h"
 #include "dcp_ptx.cuh"
 
 namespace dcp {
 namespace {
 
-constexpr uint32_t kChunk = 18432;  // divides both page sizes (73,728 and 36,864 bytes)
-constexpr int kStages = 11;
-constexpr int kLag = 8;             // loads kept ahead of stores
-static_assert(kStages - kLag - 1 >= 0, "ring too small for the lag");
-constexpr size_t kReshardSmem = (size_t)kStages * kChunk + kStages * sizeof(uint64_t);
-
 __global__ void __launch_bounds__(32, 1) reshard_kernel(const __grid_constant__ ReshardArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * kChunk);
-    __shared__ int abort_flag;
     grid_dep_wait();
     grid_dep_launch();
     if (threadIdx.x != 0) return;
-    abort_flag = 0;
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
-    fence_barrier_init();
-    fence_proxy_async_smem();
-
-    const int64_t cpp = a.page_bytes / kChunk;  // chunks per page
+    const int64_t cpp = a.page_bytes / kRingChunk;  // chunks per page
     const int64_t n_layers = a.layer_end - a.layer_begin;
     const int64_t total = n_layers * a.num_pages * cpp;
     const int64_t per = (total + gridDim.x - 1) / gridDim.x;
     const int64_t c_begin = (int64_t)blockIdx.x * per;
     const int64_t c_end = c_begin + per < total ? c_begin + per : total;
-
-    uint8_t *store_dst[kStages] = {};
-    int64_t issued = 0, stored = 0;
-    bool ok = true;
     int r = 0;
-
-    auto store_one = [&]() -> bool {
-        const int stage = (int)(stored % kStages);
-        const uint32_t parity = (uint32_t)((stored / kStages) & 1);
-        if (!mbar_wait(&bars[stage], parity, &abort_flag, a.dev_error, a.wait_limit_ns)) return false;
-        bulk_s2g(store_dst[stage], smem + (size_t)stage * kChunk, kChunk);
-        bulk_commit();
-        ++stored;
-        return true;
-    };
-
-    for (int64_t c = c_begin; c < c_end && ok; ++c) {
+    auto map = [&](int64_t c, const uint8_t *&src, uint8_t *&dst) -> bool {
         const int64_t item = c / cpp;
         const int64_t part = c - item * cpp;
         const int l = a.layer_begin + (int)(item / a.num_pages);
@@ -80,30 +53,54 @@ __global__ void __launch_bounds__(32, 1) reshard_kernel(const __grid_constant__ 
         }
         if (v < 0 || slot >= a.dst_slots || src_idx < 0 || src_idx >= a.src_pool_pages) {
             if (part == 0 && a.dev_error) atomicOr(a.dev_error, DCP_DEVERR_OUT_OF_RANGE);
-            continue;
+            return false;
         }
-        if (a.only_dst >= 0 && d != a.only_dst) continue;
-        const uint8_t *src = a.src_pools[r] +
-                             ((int64_t)(l - a.layer_start[r]) * a.src_pool_pages + src_idx) * a.page_bytes +
-                             part * kChunk;
-        uint8_t *dst = a.dst_pools[d] + ((int64_t)l * a.dst_slots + slot) * a.page_bytes + part * kChunk;
+        if (a.only_dst >= 0 && d != a.only_dst) return false;
+        src = a.src_pools[r] + ((int64_t)(l - a.layer_start[r]) * a.src_pool_pages + src_idx) * a.page_bytes +
+              part * kRingChunk;
+        dst = a.dst_pools[d] + ((int64_t)l * a.dst_slots + slot) * a.page_bytes + part * kRingChunk;
+        return true;
+    };
+    copy_ring(c_begin, c_end, map, smem, a.dev_error, a.wait_limit_ns);
+}
 
-        const int stage = (int)(issued % kStages);
-        if (issued >= kStages) bulk_wait_read<kStages - kLag - 1>();  // stage's old store has read smem
-        mbar_arrive_expect_tx(&bars[stage], kChunk);
-        bulk_g2s(smem + (size_t)stage * kChunk, src, kChunk, &bars[stage]);
-        store_dst[stage] = dst;
-        ++issued;
-        while (issued - stored > kLag && ok) ok = store_one();
-    }
-    while (ok && stored < issued) ok = store_one();
-    bulk_wait<0>();
-    if (!ok) {
-        // A load wait gave up: let the copies already issued land before the CTA exits.
-        const uint64_t t0 = global_timer_ns();
-        while (global_timer_ns() - t0 < 200000ull) {
+// Pack (to_staging) or unpack one path's items k in [item_begin, item_begin + n_items):
+// layer j = k / n_idx, list entry i = k % n_idx; staging page k - item_begin.
+__global__ void __launch_bounds__(32, 1) pack_kernel(const __grid_constant__ PackArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    grid_dep_wait();
+    grid_dep_launch();
+    if (threadIdx.x != 0) return;
+    const int64_t cpp = a.page_bytes / kRingChunk;
+    const int64_t total = a.n_items * cpp;
+    const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+    const int64_t c_begin = (int64_t)blockIdx.x * per;
+    const int64_t c_end = c_begin + per < total ? c_begin + per : total;
+    auto map = [&](int64_t c, const uint8_t *&src, uint8_t *&dst) -> bool {
+        const int64_t m = c / cpp, part = c - m * cpp;  // staging page m = item item_begin + m
+        const int64_t k = a.item_begin + m;
+        const int64_t j = k / a.n_idx, i = k - j * a.n_idx;
+        const int32_t idx = __ldg(a.idx + i);
+        uint8_t *stage = a.staging + m * a.page_bytes + part * kRingChunk;
+        if (a.to_staging) {
+            if (j >= a.n_layers || idx < 0 || idx >= a.pool_pages) {
+                if (part == 0 && a.dev_error) atomicOr(a.dev_error, DCP_DEVERR_OUT_OF_RANGE);
+                return false;
+            }
+            src = a.pool + (j * a.pool_pages + idx) * a.page_bytes + part * kRingChunk;
+            dst = stage;
+        } else {
+            const int64_t l = a.layer_offset + j;
+            if (j >= a.n_layers || l < 0 || l >= a.pool_layers || idx < 0 || idx >= a.pool_pages) {
+                if (part == 0 && a.dev_error) atomicOr(a.dev_error, DCP_DEVERR_OUT_OF_RANGE);
+                return false;
+            }
+            src = stage;
+            dst = a.pool + (l * a.pool_pages + idx) * a.page_bytes + part * kRingChunk;
         }
-    }
+        return true;
+    };
+    copy_ring(c_begin, c_end, map, smem, a.dev_error, a.wait_limit_ns);
 }
 
 // Stable single-block compaction: keep entries whose decode-side page value belongs to rank d.
@@ -174,9 +171,18 @@ filter_kernel(int64_t n, const int32_t *__restrict__ dst_vpages,
 cudaError_t launch_reshard(const ReshardArgs &a, int num_sms, cudaStream_t stream) {
     if ((a.layer_end - a.layer_begin) <= 0 || a.num_pages <= 0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(reshard_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)kReshardSmem);
+                                         (int)kRingSmem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(reshard_kernel, dim3(num_sms), dim3(32), kReshardSmem, stream, a);
+    return launch_pdl(reshard_kernel, dim3(num_sms), dim3(32), kRingSmem, stream, a);
+}
+
+cudaError_t launch_pack(const PackArgs &a, int num_sms, cudaStream_t stream) {
+    if (a.n_items <= 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(pack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem);
+    if (e != cudaSuccess) return e;
+    const int64_t chunks = a.n_items * (a.page_bytes / kRingChunk);
+    const int grid = (int)(chunks < num_sms ? chunks : num_sms);
+    return launch_pdl(pack_kernel, dim3(grid), dim3(32), kRingSmem, stream, a);
 }
 
 cudaError_t launch_filter(int64_t n, const int32_t *dst_vpages, const int32_t *transfer_idx,

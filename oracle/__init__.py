@@ -75,6 +75,10 @@ def _load():
                                            i64, i32, vp, i64, vp, vp]
             lib.dcpo_attention.restype = i32
             lib.dcpo_lse_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp]
+            lib.dcpo_pack.argtypes = [i64, vp, i32, i64, i64, i64, vp, i64, vp]
+            lib.dcpo_pack.restype = i32
+            lib.dcpo_unpack.argtypes = [i64, vp, i32, i32, i64, i64, i64, vp, vp, i32, i64]
+            lib.dcpo_unpack.restype = i32
             _lib = lib
     return _lib
 
@@ -132,6 +136,25 @@ def reshard(req_page_ptr, src_pages, dst_vpages, page_bytes: int, n_layers: int,
                                     n_layers, len(src_pools), ctypes.addressof(sarr),
                                     src_pool_pages, n_dcp, ctypes.addressof(darr), dst_slots,
                                     only_src, only_dst))
+
+
+def pack(src_idx, n_layers: int, item_begin: int, n_items: int, page_bytes: int, src_pool: np.ndarray,
+         src_pool_pages: int, staging: np.ndarray) -> int:
+    """Bounded-pack send side: items [item_begin, item_begin + n_items) of one path into staging."""
+    si = _c(src_idx, np.int32)
+    assert src_pool.dtype == np.uint8 and staging.dtype == np.uint8
+    assert staging.size >= n_items * page_bytes and src_pool.flags["C_CONTIGUOUS"] and staging.flags["C_CONTIGUOUS"]
+    return int(_load().dcpo_pack(si.size, _ptr(si), n_layers, item_begin, n_items, page_bytes, _ptr(src_pool),
+                                 src_pool_pages, _ptr(staging)))
+
+
+def unpack(dst_slot, n_layers: int, layer_offset: int, item_begin: int, n_items: int, page_bytes: int,
+           staging: np.ndarray, dst_pool: np.ndarray, num_layers: int, dst_slots: int) -> int:
+    """Bounded-pack receive side: the same item range from staging into the destination pool."""
+    ds = _c(dst_slot, np.int32)
+    assert dst_pool.dtype == np.uint8 and dst_pool.flags["C_CONTIGUOUS"]
+    return int(_load().dcpo_unpack(ds.size, _ptr(ds), n_layers, layer_offset, item_begin, n_items, page_bytes,
+                                   _ptr(staging), _ptr(dst_pool), num_layers, dst_slots))
 
 
 def bf16_value(bits: int) -> float:

@@ -225,6 +225,81 @@ def test_reshard_rejects_out_of_range_slot():
     assert st == -2
 
 
+def _path_case(seed=7):
+    """5 layers split over 2 CP ranks, 3 DCP ranks, ragged requests; tagged source pages."""
+    rng = np.random.default_rng(seed)
+    n_layers, n_cp, n_dcp = 5, 2, 3
+    lens = [64 * 7, 1, 190, 2000]
+    pages = [(n + 63) // 64 for n in lens]
+    total = sum(pages)
+    ranges = [oracle.layer_range(n_layers, n_cp, r) for r in range(n_cp)]
+    counts = [e - s for s, e in ranges]
+    ptr = np.concatenate([[0], np.cumsum(pages)]).astype(np.int64)
+    slots = total // n_dcp + 4
+    g = torch.Generator().manual_seed(seed)
+    _, vp = di.page_table(lens, n_dcp, slots, g)
+    src_pool_pages = total + 3
+    src_pages = rng.permutation(src_pool_pages)[:total].astype(np.int32)
+    page_bytes = 96
+    src = _tagged_source(pages, counts, page_bytes, src_pool_pages, rng)
+    return dict(n_layers=n_layers, n_cp=n_cp, n_dcp=n_dcp, ranges=ranges, counts=counts, ptr=ptr, slots=slots,
+                vp=vp.numpy(), src_pages=src_pages, src_pool_pages=src_pool_pages, page_bytes=page_bytes, src=src)
+
+
+@pytest.mark.parametrize("cap", [1, 7, "layer", "all", "all+3"])
+def test_pack_unpack_chunks_compose_to_path_reshard(cap):
+    """Bounded pack ([P3]): packing a path's pages chunk by chunk into a fixed staging buffer and
+    unpacking each chunk gives exactly the path's reshard ([P1] 2, 6.3); every staging page holds
+    the source page of its item (layer-major order, checked by the source tags); the bytes moved
+    equal items x page bytes whatever the buffer size, and one chunk suffices exactly when the
+    items fit (the pack trigger: pages x item bytes > buffer bytes)."""
+    c = _path_case()
+    pb = c["page_bytes"]
+    for r, d in itertools.product(range(c["n_cp"]), range(c["n_dcp"])):
+        src_idx, dst_slot = oracle.transfer_filter(c["src_pages"], c["vp"], c["n_dcp"], d)
+        n_idx = src_idx.size
+        n_items = c["counts"][r] * n_idx
+        per = {"layer": n_idx, "all": n_items, "all+3": n_items + 3}.get(cap, cap)
+        per = max(per, 1)
+        staging = np.zeros(per * pb, np.uint8)
+        got = [np.full(c["n_layers"] * c["slots"] * pb, di.SENTINEL_BYTE, np.uint8) for _ in range(c["n_dcp"])]
+        moved, n_chunks = 0, 0
+        for begin in range(0, n_items, per):
+            n = min(per, n_items - begin)
+            staging[:] = 0
+            assert oracle.pack(src_idx, c["counts"][r], begin, n, pb, c["src"][r], c["src_pool_pages"], staging) == 0
+            for m in range(n):
+                k = begin + m
+                j, i = divmod(k, n_idx)
+                tag = np.frombuffer(staging[m * pb:m * pb + 8].tobytes(), np.int16)
+                assert list(tag) == [r, j, src_idx[i], 0x51]
+            assert oracle.unpack(dst_slot, c["counts"][r], c["ranges"][r][0], begin, n, pb, staging, got[d],
+                                 c["n_layers"], c["slots"]) == 0
+            moved += n * pb
+            n_chunks += 1
+        assert moved == n_items * pb
+        assert n_chunks == -(-n_items // per)
+        assert (n_chunks == 1) == (n_items * pb <= per * pb)
+        ref = [np.full(c["n_layers"] * c["slots"] * pb, di.SENTINEL_BYTE, np.uint8) for _ in range(c["n_dcp"])]
+        assert oracle.reshard(c["ptr"], c["src_pages"], c["vp"], pb, c["n_layers"], c["src"], c["src_pool_pages"],
+                              c["n_dcp"], ref, c["slots"], only_src=r, only_dst=d) == 0
+        for a, b in zip(got, ref):
+            assert np.array_equal(a, b)
+
+
+def test_pack_rejects_out_of_range_index_and_copies_the_rest():
+    pb = 32
+    src = np.arange(3 * 4 * pb, dtype=np.uint8) % 251  # 3 layers x 4 pages
+    src_idx = np.array([2, 9, 0], np.int32)             # entry 1 is past the pool
+    staging = np.full(4 * pb, 7, np.uint8)
+    assert oracle.pack(src_idx, 3, 2, 4, pb, src, 4, staging) == -2   # items 2..5
+    v = src.reshape(3, 4, pb)
+    assert np.array_equal(staging[0:pb], v[0, 0])       # item 2: layer 0, entry 2
+    assert np.array_equal(staging[pb:2 * pb], v[1, 2])  # item 3: layer 1, entry 0
+    assert (staging[2 * pb:3 * pb] == 7).all()          # item 4: layer 1, entry 1 (skipped)
+    assert np.array_equal(staging[3 * pb:], v[1, 0])    # item 5: layer 1, entry 2
+
+
 # ------------------------------------------------------------------------------- decoders
 def test_bf16_decode_matches_format_and_torch():
     """BF16 = upper half of binary32: known encodings, and all 65536 codes vs torch's cast."""
