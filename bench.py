@@ -132,9 +132,11 @@ class Workload:
     per-step algorithmic bytes.  A step = reshard all layers, then per layer partial attention
     on every DCP rank and the LSE merge."""
 
-    def __init__(self, name: str, device, seed: int = 1, fused: bool = True, staging_mb: int = 0):
+    def __init__(self, name: str, device, seed: int = 1, fused: bool = True, staging_mb: int = 0,
+                 naive: bool = False):
         import decode_context_paged_gb300 as dcp
         self.fused = fused
+        self.naive = naive  # reshard stage as the pages' initial design: full transfer, then in-place shard
         self.pack = staging_mb > 0  # reshard stage in bounded pack mode (per path: filter, pack, unpack)
         lens_fn, self.H, self.T, self.N, self.dtype, self.L, self.n_cp, slots = WORKLOADS[name]
         lens = lens_fn()
@@ -171,6 +173,16 @@ class Workload:
                      + (f"-L{self.L}-cp{self.n_cp}" if self.L > 1 else ""))
         # reshard + per layer: plan count (+ FP8 Q split), plan build, attention, chunk combine, merge
         self.launches_per_step = 1 + self.L * 5
+        if self.naive:
+            n_pages = self.rc.dst_vpages.numel()
+            need = self.N * self.L * n_pages * self.rc.page_bytes
+            if need > (96 << 30):
+                raise SystemExit(f"--naive needs {need / 2**30:.0f} GiB of receive buffers for this workload")
+            self.recv = [torch.empty((self.L, n_pages, 64, 576), dtype=self.rc.src_pools[0].dtype, device=device)
+                         for _ in range(self.N)]
+            self.launches_per_step += 1
+            # full transfer: N x (read + write) of the KV; in-place shard: read + write once
+            self.naive_moved_bytes = (self.N + 1) * self.bytes["reshard"]
         if self.pack:
             # per path (r, d): its filtered page count (fixed by the page table, known to the host as in
             # the pages' sender) and the chunk item ranges through the bounded staging buffer
@@ -214,7 +226,14 @@ class Workload:
                     dcp.unpack_pages(slot, n_idx, cnt, start, begin, n, self.staging, rc.dst_pools[d],
                                      dev_error=self.err)
 
-        if self.pack:
+        def naive_reshard():
+            dcp.naive_full_transfer(rc.src_pages, self.L, rc.src_pools, rc.src_pool_pages, self.recv,
+                                    dev_error=self.err)
+            dcp.naive_inplace_shard(rc.dst_vpages, self.L, self.recv, rc.dst_pools, rc.dst_slots, dev_error=self.err)
+
+        if self.naive:
+            rec("reshard", naive_reshard)
+        elif self.pack:
             rec("reshard", pack_reshard)
         else:
             rec("reshard", lambda: dcp.reshard_pages(rc.req_page_ptr, rc.src_pages, rc.dst_vpages, self.L,
@@ -346,7 +365,8 @@ def run_ours(args):
     dist, rank, world, local = dist_setup()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    wl = Workload(args.config, dev, seed=1 + rank, fused=not args.unfused, staging_mb=args.staging_mb)
+    wl = Workload(args.config, dev, seed=1 + rank, fused=not args.unfused, staging_mb=args.staging_mb,
+                  naive=args.naive)
     stream = torch.cuda.current_stream()
 
     for _ in range(max(args.warmup, 3)):
@@ -443,7 +463,11 @@ def run_ours(args):
                         **({"mode": f"bounded pack, {args.staging_mb} MB staging buffer",
                             "moved_GB/s": wl.pack_moved_bytes / (stage_ms["reshard"] * 1e-3) / 1e9,
                             "moved_frac_hbm": wl.pack_moved_bytes / (stage_ms["reshard"] * 1e-3) / 1e9 / hbm}
-                           if wl.pack else {"mode": "direct"})},
+                           if wl.pack else
+                           {"mode": "naive: full transfer to every DCP rank + in-place shard",
+                            "moved_GB/s": wl.naive_moved_bytes / (stage_ms["reshard"] * 1e-3) / 1e9,
+                            "moved_frac_hbm": wl.naive_moved_bytes / (stage_ms["reshard"] * 1e-3) / 1e9 / hbm}
+                           if wl.naive else {"mode": "direct"})},
             "attn": {"ms": stage_ms["attn"], "GB/s": stage_gbs["attn"], "TFLOP/s": attn_tflops,
                      "frac_hbm": stage_gbs["attn"] / hbm, "frac_tensor": attn_tflops / tc_peak, "bound": attn_bound,
                      "includes_merge": wl.fused},
@@ -472,6 +496,8 @@ def main():
     ap.add_argument("--config", choices=sorted(WORKLOADS), default="batch")
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--naive", action="store_true",
+                    help="reshard as the pages' initial design: full KV to every DCP rank, then an in-place shard")
     ap.add_argument("--staging-mb", type=int, default=0,
                     help="reshard in bounded pack mode through a staging buffer of this many MB (0: direct)")
     ap.add_argument("--unfused", action="store_true",

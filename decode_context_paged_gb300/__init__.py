@@ -56,6 +56,10 @@ def _load():
         lib.dcp_layer_range.argtypes = [i32, i32, i32, vp, vp]
         lib.dcp_layer_range.restype = i32
         lib.dcp_filter_page_indices.argtypes = [i64, vp, vp, i32, i32, vp, vp, vp, vp]
+        lib.dcp_naive_full_transfer.argtypes = [i64, vp, i32, i32, i32, vp, i64, i32, vp, vp, vp]
+        lib.dcp_naive_full_transfer.restype = i32
+        lib.dcp_naive_inplace_shard.argtypes = [i64, vp, i32, i32, i32, vp, vp, i64, vp, vp]
+        lib.dcp_naive_inplace_shard.restype = i32
         lib.dcp_pack_pages.argtypes = [i64, vp, i32, i64, i64, i32, vp, i64, vp, sz, vp, vp]
         lib.dcp_pack_pages.restype = i32
         lib.dcp_unpack_pages.argtypes = [i64, vp, i32, i32, i64, i64, i32, vp, sz, vp, i32, i64, vp, vp]
@@ -153,6 +157,32 @@ def filter_page_indices(dst_vpages: torch.Tensor, n_dcp: int, d: int,
                                            _dptr(count, "count"), _stream(stream)),
            "dcp_filter_page_indices")
     return out_slot, out_src, count
+
+
+def naive_full_transfer(src_pages: torch.Tensor, num_layers: int, src_pools: list, src_pool_pages: int,
+                        recv_bufs: list, dev_error: torch.Tensor | None = None, stream=None) -> None:
+    """Baseline: every page of every layer to every DCP rank's receive buffer [L][pages][64][576]."""
+    dtype = _kv_code(src_pools[0])
+    sp = _ptr_array(src_pools, "src_pools")
+    rp = _ptr_array(recv_bufs, "recv_bufs")
+    _check(_load().dcp_naive_full_transfer(src_pages.numel(), _dptr(src_pages, "src_pages", torch.int32), dtype,
+                                           num_layers, len(src_pools), ctypes.addressof(sp), src_pool_pages,
+                                           len(recv_bufs), ctypes.addressof(rp),
+                                           _dptr(dev_error, "dev_error", torch.int32), _stream(stream)),
+           "dcp_naive_full_transfer")
+
+
+def naive_inplace_shard(dst_vpages: torch.Tensor, num_layers: int, recv_bufs: list, dst_pools: list,
+                        dst_slots_per_rank: int, dev_error: torch.Tensor | None = None, stream=None) -> None:
+    """Baseline: each rank keeps the pages it owns from its full copy, at their DCP slots."""
+    dtype = _kv_code(dst_pools[0])
+    rp = _ptr_array(recv_bufs, "recv_bufs")
+    dp = _ptr_array(dst_pools, "dst_pools")
+    _check(_load().dcp_naive_inplace_shard(dst_vpages.numel(), _dptr(dst_vpages, "dst_vpages", torch.int32), dtype,
+                                           num_layers, len(dst_pools), ctypes.addressof(rp), ctypes.addressof(dp),
+                                           dst_slots_per_rank, _dptr(dev_error, "dev_error", torch.int32),
+                                           _stream(stream)),
+           "dcp_naive_inplace_shard")
 
 
 def pack_chunks(n_items: int, page_bytes: int, staging_bytes: int) -> list:

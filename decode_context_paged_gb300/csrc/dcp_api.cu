@@ -135,6 +135,76 @@ int dcp_reshard_pages(int num_requests, const int64_t *req_page_ptr, int64_t num
     return DCP_OK;
 }
 
+int dcp_naive_full_transfer(int64_t num_pages, const int32_t *src_pages, int dtype, int num_layers, int n_cp,
+                            const void *const *src_pools, int64_t src_pool_pages, int n_dcp, void *const *recv_bufs,
+                            int32_t *dev_error, dcp_stream_t stream) {
+    if (num_pages < 0 || num_layers < 0 || src_pool_pages < 0) return DCP_ERR_INVALID_ARG;
+    if (dtype != DCP_KV_BF16 && dtype != DCP_KV_FP8_E4M3) return DCP_ERR_INVALID_ARG;
+    if (n_cp < 1 || n_cp > kMaxCp || n_dcp < 1 || n_dcp > kMaxDcpReshard) return DCP_ERR_INVALID_ARG;
+    if (num_pages == 0 || num_layers == 0) return DCP_OK;
+    if (!src_pages || !src_pools || !recv_bufs) return DCP_ERR_INVALID_ARG;
+    NaiveArgs na{};
+    ReshardArgs &a = na.base;
+    a.src_pages = src_pages;
+    a.num_pages = num_pages;
+    a.page_bytes = (int64_t)kPage * kKDim * (dtype == DCP_KV_BF16 ? 2 : 1);
+    a.n_cp = n_cp;
+    for (int r = 0; r < n_cp; ++r) {
+        int s0, e0;
+        layer_range(num_layers, n_cp, r, &s0, &e0);
+        a.layer_start[r] = s0;
+        a.layer_start[r + 1] = e0;
+        a.src_pools[r] = static_cast<const uint8_t *>(src_pools[r]);
+        if ((e0 > s0) && (!src_pools[r] || !aligned(src_pools[r], 16))) return DCP_ERR_INVALID_ARG;
+    }
+    a.layer_begin = 0;
+    a.layer_end = num_layers;
+    a.src_pool_pages = src_pool_pages;
+    a.n_dcp = n_dcp;
+    for (int d = 0; d < n_dcp; ++d) {
+        if (!recv_bufs[d] || !aligned(recv_bufs[d], 16)) return DCP_ERR_INVALID_ARG;
+        na.recv[d] = static_cast<uint8_t *>(recv_bufs[d]);
+    }
+    a.dev_error = dev_error;
+    a.wait_limit_ns = wait_limit_ns();
+    na.mode = 0;
+    int sms = 0;
+    if (int st = current_sm_count(&sms)) return st;
+    return launch_naive(na, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
+int dcp_naive_inplace_shard(int64_t num_pages, const int32_t *dst_vpages, int dtype, int num_layers, int n_dcp,
+                            const void *const *recv_bufs, void *const *dst_pools, int64_t dst_slots_per_rank,
+                            int32_t *dev_error, dcp_stream_t stream) {
+    if (num_pages < 0 || num_layers < 0 || dst_slots_per_rank < 0) return DCP_ERR_INVALID_ARG;
+    if (dtype != DCP_KV_BF16 && dtype != DCP_KV_FP8_E4M3) return DCP_ERR_INVALID_ARG;
+    if (n_dcp < 1 || n_dcp > kMaxDcpReshard) return DCP_ERR_INVALID_ARG;
+    if (num_pages == 0 || num_layers == 0) return DCP_OK;
+    if (!dst_vpages || !recv_bufs || !dst_pools) return DCP_ERR_INVALID_ARG;
+    NaiveArgs na{};
+    ReshardArgs &a = na.base;
+    a.dst_vpages = dst_vpages;
+    a.num_pages = num_pages;
+    a.page_bytes = (int64_t)kPage * kKDim * (dtype == DCP_KV_BF16 ? 2 : 1);
+    a.n_cp = 1;
+    a.layer_begin = 0;
+    a.layer_end = num_layers;
+    a.n_dcp = n_dcp;
+    for (int d = 0; d < n_dcp; ++d) {
+        if (!recv_bufs[d] || !aligned(recv_bufs[d], 16) || !dst_pools[d] || !aligned(dst_pools[d], 16))
+            return DCP_ERR_INVALID_ARG;
+        na.recv[d] = static_cast<uint8_t *>(const_cast<void *>(recv_bufs[d]));
+        a.dst_pools[d] = static_cast<uint8_t *>(dst_pools[d]);
+    }
+    a.dst_slots = dst_slots_per_rank;
+    a.dev_error = dev_error;
+    a.wait_limit_ns = wait_limit_ns();
+    na.mode = 1;
+    int sms = 0;
+    if (int st = current_sm_count(&sms)) return st;
+    return launch_naive(na, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
 static int pack_impl(int64_t n_idx, const int32_t *idx, int n_layers, int layer_offset, int64_t item_begin,
                      int64_t n_items, int dtype, const void *pool, int64_t pool_pages, int pool_layers,
                      const void *staging, size_t staging_bytes, int to_staging, int32_t *dev_error,

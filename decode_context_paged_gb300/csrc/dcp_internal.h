@@ -61,6 +61,14 @@ struct ReshardArgs {
 };
 cudaError_t launch_reshard(const ReshardArgs &a, int num_sms, cudaStream_t stream);
 
+// ---- the naive baseline: full transfer to every DCP rank, then an in-place shard (dcp_reshard.cu)
+struct NaiveArgs {
+    ReshardArgs base;                     // page table, layer split, source and destination pools
+    uint8_t *recv[kMaxDcpReshard];        // per DCP rank: [num_layers][num_pages] receive buffer
+    int mode;                             // 0 = full transfer, 1 = in-place shard
+};
+cudaError_t launch_naive(const NaiveArgs &a, int num_sms, cudaStream_t stream);
+
 // ---- pack / unpack of one path's pages through a staging buffer (dcp_reshard.cu)
 struct PackArgs {
     const int32_t *idx;      // [n_idx]: source page indices (pack) or destination slots (unpack)

@@ -64,6 +64,57 @@ __global__ void __launch_bounds__(32, 1) reshard_kernel(const __grid_constant__ 
     copy_ring(c_begin, c_end, map, smem, a.dev_error, a.wait_limit_ns);
 }
 
+// The pages' initial design, kept as a bandwidth baseline ("Design Evolution", 6.1).
+// Mode 0 (full transfer): every page entry of every layer to every DCP rank's receive buffer
+// [layer][page entry] (N_dcp times the KV).  Mode 1 (in-place shard): each page entry of each
+// layer from its owner's receive buffer to the owner's DCP slot.
+__global__ void __launch_bounds__(32, 1) naive_kernel(const __grid_constant__ NaiveArgs na) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    grid_dep_wait();
+    grid_dep_launch();
+    if (threadIdx.x != 0) return;
+    const ReshardArgs &a = na.base;
+    const int64_t cpp = a.page_bytes / kRingChunk;
+    const int64_t lp = (int64_t)a.layer_end * a.num_pages;  // (layer, entry) items of one rank
+    const int n_dst = a.n_dcp <= 1 ? 1 : a.n_dcp;
+    const int64_t total = (na.mode == 0 ? n_dst : 1) * lp * cpp;
+    const int64_t per = (total + gridDim.x - 1) / gridDim.x;
+    const int64_t c_begin = (int64_t)blockIdx.x * per;
+    const int64_t c_end = c_begin + per < total ? c_begin + per : total;
+    int r = 0;
+    auto map = [&](int64_t c, const uint8_t *&src, uint8_t *&dst) -> bool {
+        const int64_t item = c / cpp, part = c - item * cpp;
+        const int64_t li = item % lp;  // layer * num_pages + entry
+        const int l = (int)(li / a.num_pages);
+        const int64_t i = li - (int64_t)l * a.num_pages;
+        if (na.mode == 0) {
+            const int d = (int)(item / lp);
+            while (r + 1 < a.n_cp && l >= a.layer_start[r + 1]) ++r;
+            while (r > 0 && l < a.layer_start[r]) --r;
+            const int32_t s_idx = __ldg(a.src_pages + i);
+            if (s_idx < 0 || s_idx >= a.src_pool_pages) {
+                if (part == 0 && a.dev_error) atomicOr(a.dev_error, DCP_DEVERR_OUT_OF_RANGE);
+                return false;
+            }
+            src = a.src_pools[r] + ((int64_t)(l - a.layer_start[r]) * a.src_pool_pages + s_idx) * a.page_bytes +
+                  part * kRingChunk;
+            dst = na.recv[d] + li * a.page_bytes + part * kRingChunk;
+            return true;
+        }
+        const int32_t v = __ldg(a.dst_vpages + i);
+        const int d = a.n_dcp <= 1 ? 0 : v % a.n_dcp;
+        const int64_t slot = a.n_dcp <= 1 ? (int64_t)v : (int64_t)(v / a.n_dcp);
+        if (v < 0 || slot >= a.dst_slots) {
+            if (part == 0 && a.dev_error) atomicOr(a.dev_error, DCP_DEVERR_OUT_OF_RANGE);
+            return false;
+        }
+        src = na.recv[d] + li * a.page_bytes + part * kRingChunk;
+        dst = a.dst_pools[d] + ((int64_t)l * a.dst_slots + slot) * a.page_bytes + part * kRingChunk;
+        return true;
+    };
+    copy_ring(c_begin, c_end, map, smem, a.dev_error, a.wait_limit_ns);
+}
+
 // Pack (to_staging) or unpack one path's items k in [item_begin, item_begin + n_items):
 // layer j = k / n_idx, list entry i = k % n_idx; staging page k - item_begin.
 __global__ void __launch_bounds__(32, 1) pack_kernel(const __grid_constant__ PackArgs a) {
@@ -174,6 +225,13 @@ cudaError_t launch_reshard(const ReshardArgs &a, int num_sms, cudaStream_t strea
                                          (int)kRingSmem);
     if (e != cudaSuccess) return e;
     return launch_pdl(reshard_kernel, dim3(num_sms), dim3(32), kRingSmem, stream, a);
+}
+
+cudaError_t launch_naive(const NaiveArgs &a, int num_sms, cudaStream_t stream) {
+    if (a.base.layer_end <= 0 || a.base.num_pages <= 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(naive_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(naive_kernel, dim3(num_sms), dim3(32), kRingSmem, stream, a);
 }
 
 cudaError_t launch_pack(const PackArgs &a, int num_sms, cudaStream_t stream) {

@@ -133,6 +133,28 @@ int dcp_reshard_pages(int num_requests, const int64_t *req_page_ptr, int64_t num
                       int only_dst_rank, int32_t *dev_error, dcp_stream_t stream);
 
 /*
+ * [P1] 6.1 "Design Evolution", the initial design, kept as the bandwidth baseline of the 2D
+ * reshard: prefill sends the full, unsharded KV to every decode DCP rank, then each rank keeps
+ * the pages it owns (the in-place shard).  The two calls together leave dst_pools exactly as
+ * dcp_reshard_pages does, after moving n_dcp times the KV instead of once ([P1] 6.1: 4x at
+ * DCP=4, 75% of it discarded).
+ *   dcp_naive_full_transfer: recv_bufs[d][l][i] <- src_pools[r][l - start_r][src_pages[i]] for
+ *     every DCP rank d, layer l (owned by CP rank r per dcp_layer_range) and page entry i.
+ *   dcp_naive_inplace_shard: dst_pools[d][l][v div n_dcp] <- recv_bufs[d][l][i] for the entries
+ *     whose page value v = dst_vpages[i] has v mod n_dcp == d.
+ * recv_bufs: HOST array [n_dcp] of device pointers, each [num_layers][num_pages][64][576]
+ * (16-byte aligned); the other arguments as in dcp_reshard_pages (page entries of all requests
+ * concatenated, num_pages of them).  Out-of-range indices set DCP_DEVERR_OUT_OF_RANGE and skip
+ * the page.  Returns DCP_ERR_INVALID_ARG, DCP_ERR_CUDA.
+ */
+int dcp_naive_full_transfer(int64_t num_pages, const int32_t *src_pages, int dtype, int num_layers,
+                            int n_cp, const void *const *src_pools, int64_t src_pool_pages, int n_dcp,
+                            void *const *recv_bufs, int32_t *dev_error, dcp_stream_t stream);
+int dcp_naive_inplace_shard(int64_t num_pages, const int32_t *dst_vpages, int dtype, int num_layers,
+                            int n_dcp, const void *const *recv_bufs, void *const *dst_pools,
+                            int64_t dst_slots_per_rank, int32_t *dev_error, dcp_stream_t stream);
+
+/*
  * Bounded pack mode of one reshard path (source rank r -> destination rank d): the review of
  * the bounded pack buffer ([P3]: the sender gathers a path's pages into a fixed, pre-registered
  * staging buffer and, when they do not fit at once, reuses it chunk after chunk; the bytes

@@ -75,6 +75,10 @@ def _load():
                                            i64, i32, vp, i64, vp, vp]
             lib.dcpo_attention.restype = i32
             lib.dcpo_lse_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp]
+            lib.dcpo_full_transfer.argtypes = [i64, vp, i64, i32, i32, vp, i64, i32, vp]
+            lib.dcpo_full_transfer.restype = i32
+            lib.dcpo_inplace_shard.argtypes = [i64, vp, i64, i32, i32, vp, vp, i64]
+            lib.dcpo_inplace_shard.restype = i32
             lib.dcpo_pack.argtypes = [i64, vp, i32, i64, i64, i64, vp, i64, vp]
             lib.dcpo_pack.restype = i32
             lib.dcpo_unpack.argtypes = [i64, vp, i32, i32, i64, i64, i64, vp, vp, i32, i64]
@@ -136,6 +140,30 @@ def reshard(req_page_ptr, src_pages, dst_vpages, page_bytes: int, n_layers: int,
                                     n_layers, len(src_pools), ctypes.addressof(sarr),
                                     src_pool_pages, n_dcp, ctypes.addressof(darr), dst_slots,
                                     only_src, only_dst))
+
+
+def full_transfer(src_pages, page_bytes: int, n_layers: int, src_pools: list, src_pool_pages: int, n_dcp: int,
+                  recv: list) -> int:
+    """Naive transfer: every page of every layer to every DCP rank's receive buffer [L][pages]."""
+    sp = _c(src_pages, np.int32)
+    for p in list(src_pools) + list(recv):
+        assert p.dtype == np.uint8 and p.flags["C_CONTIGUOUS"]
+    sarr = (ctypes.c_void_p * len(src_pools))(*[_ptr(p) for p in src_pools])
+    rarr = (ctypes.c_void_p * len(recv))(*[_ptr(p) for p in recv])
+    return int(_load().dcpo_full_transfer(sp.size, _ptr(sp), page_bytes, n_layers, len(src_pools),
+                                          ctypes.addressof(sarr), src_pool_pages, n_dcp, ctypes.addressof(rarr)))
+
+
+def inplace_shard(dst_vpages, page_bytes: int, n_layers: int, n_dcp: int, recv: list, dst_pools: list,
+                  dst_slots: int) -> int:
+    """Each rank keeps the pages it owns from its full copy, at their DCP slots."""
+    dv = _c(dst_vpages, np.int32)
+    for p in list(recv) + list(dst_pools):
+        assert p.dtype == np.uint8 and p.flags["C_CONTIGUOUS"]
+    rarr = (ctypes.c_void_p * len(recv))(*[_ptr(p) for p in recv])
+    darr = (ctypes.c_void_p * len(dst_pools))(*[_ptr(p) for p in dst_pools])
+    return int(_load().dcpo_inplace_shard(dv.size, _ptr(dv), page_bytes, n_layers, n_dcp, ctypes.addressof(rarr),
+                                          ctypes.addressof(darr), dst_slots))
 
 
 def pack(src_idx, n_layers: int, item_begin: int, n_items: int, page_bytes: int, src_pool: np.ndarray,

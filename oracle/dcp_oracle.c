@@ -311,6 +311,60 @@ int dcpo_attention(int num_requests, int q_len, int num_heads, const uint16_t *q
 /* zero; if every part is -inf the row is empty: O = 0, LSE = -inf.                       */
 /* Layouts: o_part [n_parts][rows][v_dim], lse_part [n_parts][rows].                      */
 /* ------------------------------------------------------------------------------------ */
+/* [P1] 6.1 "Design Evolution", the initial approach: prefill sends the full, unsharded KV  */
+/* to every decode DCP rank (each receives N_dcp times the data it needs), then each rank   */
+/* runs an in-place shard keeping only the pages it owns.  Reading: the receive buffer of   */
+/* rank d is [layer][page entry] in page-table order; the shard keeps entry i at the slot   */
+/* its decode value names (owner v mod N_dcp == d, slot v div N_dcp), i.e. the 2D reshard's */
+/* result, after N_dcp times the transfer.  Out-of-range indices skip the page, return -2. */
+/* ------------------------------------------------------------------------------------ */
+int dcpo_full_transfer(int64_t num_pages, const int32_t *src_pages, int64_t page_bytes, int n_layers, int n_cp,
+                       uint8_t *const *src_pools, int64_t src_pool_pages, int n_dcp, uint8_t *const *recv) {
+    int status = 0;
+    int n_dst = n_dcp <= 1 ? 1 : n_dcp;
+    for (int d = 0; d < n_dst; ++d)
+        for (int r = 0; r < n_cp; ++r) {
+            int l0, l1;
+            dcpo_layer_range(n_layers, n_cp, r, &l0, &l1);
+            for (int l = l0; l < l1; ++l)
+                for (int64_t i = 0; i < num_pages; ++i) {
+                    if (src_pages[i] < 0 || src_pages[i] >= src_pool_pages) {
+                        status = -2;
+                        continue;
+                    }
+                    memcpy(recv[d] + ((int64_t)l * num_pages + i) * page_bytes,
+                           src_pools[r] + ((int64_t)(l - l0) * src_pool_pages + src_pages[i]) * page_bytes,
+                           (size_t)page_bytes);
+                }
+        }
+    return status;
+}
+
+int dcpo_inplace_shard(int64_t num_pages, const int32_t *dst_vpages, int64_t page_bytes, int n_layers, int n_dcp,
+                       uint8_t *const *recv, uint8_t *const *dst_pools, int64_t dst_slots) {
+    int status = 0;
+    int n_dst = n_dcp <= 1 ? 1 : n_dcp;
+    for (int d = 0; d < n_dst; ++d)
+        for (int l = 0; l < n_layers; ++l)
+            for (int64_t i = 0; i < num_pages; ++i) {
+                int32_t v = dst_vpages[i];
+                if (v < 0) {
+                    status = -2;
+                    continue;
+                }
+                if (page_owner(v, n_dcp) != d) continue;
+                int64_t slot = page_slot(v, n_dcp);
+                if (slot >= dst_slots) {
+                    status = -2;
+                    continue;
+                }
+                memcpy(dst_pools[d] + ((int64_t)l * dst_slots + slot) * page_bytes,
+                       recv[d] + ((int64_t)l * num_pages + i) * page_bytes, (size_t)page_bytes);
+            }
+    return status;
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* [P3] bounded pack buffer: the sending side gathers one path's pages into a fixed,       */
 /* pre-registered staging buffer and, when they do not fit at once (pages x item bytes >   */
 /* buffer bytes), reuses it chunk after chunk; the transferred bytes are unchanged.  The    */

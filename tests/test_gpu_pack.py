@@ -1,4 +1,5 @@
-"""GPU parity of the bounded pack mode (dcp_pack_pages / dcp_unpack_pages), bit for bit.
+"""GPU parity of the reshard's other modes, bit for bit: the bounded pack mode
+(dcp_pack_pages / dcp_unpack_pages) and the naive full-transfer + in-place-shard baseline.
 
 For every path (source rank r, destination rank d) of a multi-layer CP2 -> DCP4 reshard, the
 path's filtered page list comes from dcp_filter_page_indices on the GPU; packing its items chunk
@@ -79,3 +80,32 @@ def test_pack_out_of_range_sets_device_error(cuda_device):
     src = _u8(case.src_pools[0]).reshape(-1, pb)
     assert np.array_equal(s[:pb], src[0]) and np.array_equal(s[2 * pb:], src[1])
     assert (s[pb:2 * pb] == 7).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+def test_naive_transfer_and_inplace_shard_match_oracle_and_reshard(cuda_device, dtype):
+    """The 6.1 baseline: the receive buffers equal the oracle's full transfer bit for bit, and
+    the in-place shard leaves the DCP pools exactly as the 2D reshard does."""
+    lens = [64 * 30 + 5, 700, 64 * 3]
+    counts = [2, 2]  # 4 layers over 2 CP ranks
+    case = di.reshard_case(lens, n_layers=4, layer_counts=counts, n_dcp=4, dtype=dtype, contiguous_src=False,
+                           seed=31, device=cuda_device)
+    pb = case.page_bytes
+    n_pages = case.dst_vpages.numel()
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    recv = [torch.empty((4, n_pages, 64, 576), dtype=case.src_pools[0].dtype, device=cuda_device) for _ in range(4)]
+    dcp.naive_full_transfer(case.src_pages, 4, case.src_pools, case.src_pool_pages, recv, dev_error=err)
+    got = [_sentinel_like(p) for p in case.dst_pools]
+    dcp.naive_inplace_shard(case.dst_vpages, 4, recv, got, case.dst_slots, dev_error=err)
+    ref = [_sentinel_like(p) for p in case.dst_pools]
+    dcp.reshard_pages(case.req_page_ptr, case.src_pages, case.dst_vpages, 4, case.src_pools, case.src_pool_pages,
+                      ref, case.dst_slots, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref_recv = [np.zeros(4 * n_pages * pb, np.uint8) for _ in range(4)]
+    assert oracle.full_transfer(case.src_pages.cpu().numpy(), pb, 4, [_u8(p) for p in case.src_pools],
+                                case.src_pool_pages, 4, ref_recv) == 0
+    for a, b in zip(recv, ref_recv):
+        assert np.array_equal(_u8(a), b)
+    for a, b in zip(got, ref):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))

@@ -300,6 +300,43 @@ def test_pack_rejects_out_of_range_index_and_copies_the_rest():
     assert np.array_equal(staging[3 * pb:], v[1, 0])    # item 5: layer 1, entry 2
 
 
+@pytest.mark.parametrize("n_dcp", [1, 3, 4])
+def test_naive_transfer_then_inplace_shard_equals_2d_reshard(n_dcp):
+    """6.1: the initial design (full unsharded KV to every DCP rank, then an in-place shard)
+    ends in the same DCP layout as the 2D reshard, after N_dcp times the transfer: every rank's
+    receive buffer holds the whole sequence, and the shard discards (N_dcp - 1) / N_dcp of it."""
+    c = _path_case(seed=4)
+    pb, L = c["page_bytes"], c["n_layers"]
+    total = c["src_pages"].size
+    vp = c["vp"] if n_dcp == 3 else _table_for(c, n_dcp)
+    n_ranks = max(n_dcp, 1)
+    slots = total // n_ranks + 4
+    recv = [np.zeros(L * total * pb, np.uint8) for _ in range(n_ranks)]
+    assert oracle.full_transfer(c["src_pages"], pb, L, c["src"], c["src_pool_pages"], n_dcp, recv) == 0
+    for d in range(n_ranks):  # the whole sequence, page-table order, at every rank
+        for l in range(L):
+            r = next(i for i, (s0, e0) in enumerate(c["ranges"]) if s0 <= l < e0)
+            for i in range(total):
+                tag = np.frombuffer(recv[d][(l * total + i) * pb:(l * total + i) * pb + 8].tobytes(), np.int16)
+                assert list(tag) == [r, l - c["ranges"][r][0], c["src_pages"][i], 0x51]
+    got = [np.full(L * slots * pb, di.SENTINEL_BYTE, np.uint8) for _ in range(n_ranks)]
+    assert oracle.inplace_shard(vp, pb, L, n_dcp, recv, got, slots) == 0
+    ref = [np.full(L * slots * pb, di.SENTINEL_BYTE, np.uint8) for _ in range(n_ranks)]
+    assert oracle.reshard(c["ptr"], c["src_pages"], vp, pb, L, c["src"], c["src_pool_pages"], n_dcp, ref, slots) == 0
+    for a, b in zip(got, ref):
+        assert np.array_equal(a, b)
+    transferred = sum(x.size for x in recv)
+    assert transferred == n_ranks * L * total * pb  # N_dcp x the KV; the 2D reshard moves 1 x
+
+
+def _table_for(c, n_dcp):
+    pages = [int(c["ptr"][b + 1] - c["ptr"][b]) for b in range(len(c["ptr"]) - 1)]
+    total = sum(pages)
+    g = torch.Generator().manual_seed(23)
+    _, vp = di.page_table([64 * n for n in pages], n_dcp, total // max(n_dcp, 1) + 4, g)
+    return vp.numpy()
+
+
 # ------------------------------------------------------------------------------- decoders
 def test_bf16_decode_matches_format_and_torch():
     """BF16 = upper half of binary32: known encodings, and all 65536 codes vs torch's cast."""
