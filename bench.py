@@ -133,8 +133,10 @@ class Workload:
     on every DCP rank and the LSE merge."""
 
     def __init__(self, name: str, device, seed: int = 1, fused: bool = True, staging_mb: int = 0,
-                 naive: bool = False):
+                 naive: bool = False, layout: str = "page"):
         import decode_context_paged_gb300 as dcp
+        self.layout = layout  # "token": token-interleaved DCP (row-gather reshard, token-layout attention)
+        fused = fused and layout == "page"
         self.fused = fused
         self.naive = naive  # reshard stage as the pages' initial design: full transfer, then in-place shard
         self.pack = staging_mb > 0  # reshard stage in bounded pack mode (per path: filter, pack, unpack)
@@ -147,7 +149,19 @@ class Workload:
                                   contiguous_src=True, seed=seed, device=device, dst_slots=slots)
         self.q = di.random_q(self.B, self.T, self.H, di._gen(seed + 7, device), device)
         self.seq_lens = torch.tensor(lens, dtype=torch.int32, device=device)
-        self.layer_pools = [[p[l] for p in self.rc.dst_pools] for l in range(self.L)]
+        if layout == "token":
+            # destination: the token-interleaved table and per-rank pools (same pages per rank)
+            g = torch.Generator().manual_seed(seed + 11)
+            tslots = sum(-(-(-(-n // self.N)) // 64) for n in lens) + 1
+            tptr, tv = di.token_page_table(lens, self.N, tslots, g)
+            self.tok_ptr, self.tok_vp, self.tok_slots = tptr.to(device), tv.to(device), tslots
+            self.tok_pools = [torch.empty((self.L, tslots, 64, 576), dtype=self.rc.src_pools[0].dtype, device=device)
+                              for _ in range(self.N)]
+            for t in self.tok_pools:
+                t.view(torch.uint8).zero_()
+            self.layer_pools = [[p[l] for p in self.tok_pools] for l in range(self.L)]
+        else:
+            self.layer_pools = [[p[l] for p in self.rc.dst_pools] for l in range(self.L)]
         self.kv_scale = di.FP8_KV_SCALE if self.dtype == "e4m3" else 1.0
         self.scale = di.SOFTMAX_SCALE
         R = self.B * self.T * self.H
@@ -156,7 +170,8 @@ class Workload:
         self.lse_part = torch.empty((self.N, self.B, self.T, self.H), dtype=torch.float32, device=device)
         self.o = torch.empty((self.L, self.B, self.T, self.H, 512), dtype=torch.float32, device=device)
         self.lse = torch.empty((self.L, self.B, self.T, self.H), dtype=torch.float32, device=device)
-        self.ws = dcp.alloc_workspace(self.B, self.T, self.H, self.N, self.rc.dst_vpages.numel(), device)
+        n_entries = self.tok_vp.numel() if layout == "token" else self.rc.dst_vpages.numel()
+        self.ws = dcp.alloc_workspace(self.B, self.T, self.H, self.N, n_entries, device)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         pages = self.rc.dst_vpages.numel()
         elem = 2 if self.dtype == "bf16" else 1
@@ -231,7 +246,13 @@ class Workload:
                                     dev_error=self.err)
             dcp.naive_inplace_shard(rc.dst_vpages, self.L, self.recv, rc.dst_pools, rc.dst_slots, dev_error=self.err)
 
-        if self.naive:
+        def token_reshard():
+            dcp.token_reshard(self.seq_lens, rc.req_page_ptr, rc.src_pages, self.tok_ptr, self.tok_vp, self.L,
+                              rc.src_pools, rc.src_pool_pages, self.tok_pools, self.tok_slots, dev_error=self.err)
+
+        if self.layout == "token":
+            rec("reshard", token_reshard)
+        elif self.naive:
             rec("reshard", naive_reshard)
         elif self.pack:
             rec("reshard", pack_reshard)
@@ -246,10 +267,11 @@ class Workload:
                                                            o_part=self.o_part, lse_part=self.lse_part, o_out=self.o[l],
                                                            lse_out=self.lse[l], workspace=self.ws, dev_error=self.err))
                 continue
-            rec("attn", lambda: dcp.partial_decode_attn(self.q, self.seq_lens, rc.req_page_ptr, rc.dst_vpages,
+            tbl = (self.tok_ptr, self.tok_vp) if self.layout == "token" else (rc.req_page_ptr, rc.dst_vpages)
+            rec("attn", lambda: dcp.partial_decode_attn(self.q, self.seq_lens, tbl[0], tbl[1],
                                                         self.layer_pools[l], self.scale, self.kv_scale,
                                                         o_part=self.o_part, lse_part=self.lse_part, workspace=self.ws,
-                                                        dev_error=self.err))
+                                                        dev_error=self.err, layout=self.layout))
             rec("merge", lambda: dcp.lse_merge(self.o_part, self.lse_part, self.o[l], self.lse[l]))
 
 
@@ -366,7 +388,7 @@ def run_ours(args):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wl = Workload(args.config, dev, seed=1 + rank, fused=not args.unfused, staging_mb=args.staging_mb,
-                  naive=args.naive)
+                  naive=args.naive, layout=args.layout)
     stream = torch.cuda.current_stream()
 
     for _ in range(max(args.warmup, 3)):
@@ -467,7 +489,8 @@ def run_ours(args):
                            {"mode": "naive: full transfer to every DCP rank + in-place shard",
                             "moved_GB/s": wl.naive_moved_bytes / (stage_ms["reshard"] * 1e-3) / 1e9,
                             "moved_frac_hbm": wl.naive_moved_bytes / (stage_ms["reshard"] * 1e-3) / 1e9 / hbm}
-                           if wl.naive else {"mode": "direct"})},
+                           if wl.naive else {"mode": "token-interleaved row gather"} if wl.layout == "token"
+                           else {"mode": "direct"})},
             "attn": {"ms": stage_ms["attn"], "GB/s": stage_gbs["attn"], "TFLOP/s": attn_tflops,
                      "frac_hbm": stage_gbs["attn"] / hbm, "frac_tensor": attn_tflops / tc_peak, "bound": attn_bound,
                      "includes_merge": wl.fused},
@@ -496,6 +519,8 @@ def main():
     ap.add_argument("--config", choices=sorted(WORKLOADS), default="batch")
     ap.add_argument("--ref-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layout", choices=["page", "token"], default="page",
+                    help="token: token-interleaved DCP (rank i holds tokens i, i + N, ...) instead of pages")
     ap.add_argument("--naive", action="store_true",
                     help="reshard as the pages' initial design: full KV to every DCP rank, then an in-place shard")
     ap.add_argument("--staging-mb", type=int, default=0,

@@ -93,6 +93,27 @@ def page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Generator):
     return torch.tensor(ptr, dtype=torch.int64), vp.to(torch.int32)
 
 
+def token_page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Generator):
+    """Token-interleaved layout: rank d holds tokens d, d + N, ...; a request's table entry
+    jj * N + d names rank d's local page jj at a seeded random free slot.  Every rank gets the
+    same number of local pages, ceil(ceil(n / N) / 64).  Returns (req_page_ptr, dst_vpages)."""
+    n_ranks = max(n_dcp, 1)
+    local = [-(-(-(-int(n) // n_ranks)) // PAGE) for n in seq_lens]
+    perms = [torch.randperm(slots_per_rank, generator=gen, device="cpu") for _ in range(n_ranks)]
+    used = [0] * n_ranks
+    ptr, vp = [0], []
+    for p in local:
+        for jj in range(p):
+            for d in range(n_ranks):
+                if used[d] >= slots_per_rank:
+                    raise ValueError("pool too small for the page table")
+                slot = int(perms[d][used[d]])
+                used[d] += 1
+                vp.append(slot * n_ranks + d if n_dcp > 1 else slot)
+        ptr.append(ptr[-1] + p * n_ranks)
+    return torch.tensor(ptr, dtype=torch.int64), torch.tensor(vp, dtype=torch.int32)
+
+
 @dataclass
 class AttnCase:
     """One partial-attention workload (all tensors on ``device``)."""
@@ -110,6 +131,7 @@ class AttnCase:
     kv_scale: float
     softmax_scale: float = SOFTMAX_SCALE
     name: str = ""
+    layout: str = "page"            # "token": the table is token-interleaved (token_page_table)
 
     @property
     def rows(self) -> int:
@@ -165,6 +187,23 @@ class ReshardCase:
     @property
     def page_bytes(self) -> int:
         return PAGE * K_DIM * (2 if self.dtype == "bf16" else 1)
+
+
+def token_attention_case(seq_lens, H: int, T: int, n_dcp: int, dtype: str, seed: int, device,
+                         name: str = "") -> AttnCase:
+    """An attention workload over the token-interleaved layout (token_page_table)."""
+    gen_cpu = _gen(seed, "cpu")
+    gen_dev = _gen(seed + 1000003, device)
+    seq_lens = [int(n) for n in seq_lens]
+    n_ranks = max(n_dcp, 1)
+    slots = max(1, sum(-(-(-(-n // n_ranks)) // PAGE) for n in seq_lens))
+    ptr, vp = token_page_table(seq_lens, n_dcp, slots, gen_cpu)
+    q = random_q(len(seq_lens), T, H, gen_dev, device)
+    pools = [random_pool(slots, dtype, gen_dev, device) for _ in range(n_ranks)]
+    return AttnCase(B=len(seq_lens), T=T, H=H, n_dcp=n_dcp, dtype=dtype,
+                    seq_lens=torch.tensor(seq_lens, dtype=torch.int32, device=device),
+                    req_page_ptr=ptr.to(device), dst_vpages=vp.to(device), q=q, pools=pools, slots_per_rank=slots,
+                    kv_scale=FP8_KV_SCALE if dtype == "e4m3" else 1.0, name=name, layout="token")
 
 
 SENTINEL_BYTE = 0xA5

@@ -56,6 +56,8 @@ def _load():
         lib.dcp_layer_range.argtypes = [i32, i32, i32, vp, vp]
         lib.dcp_layer_range.restype = i32
         lib.dcp_filter_page_indices.argtypes = [i64, vp, vp, i32, i32, vp, vp, vp, vp]
+        lib.dcp_token_reshard.argtypes = [i32, vp, vp, vp, vp, i64, vp, i32, i32, i32, vp, i64, i32, vp, i64, vp, vp]
+        lib.dcp_token_reshard.restype = i32
         lib.dcp_naive_full_transfer.argtypes = [i64, vp, i32, i32, i32, vp, i64, i32, vp, vp, vp]
         lib.dcp_naive_full_transfer.restype = i32
         lib.dcp_naive_inplace_shard.argtypes = [i64, vp, i32, i32, i32, vp, vp, i64, vp, vp]
@@ -73,6 +75,8 @@ def _load():
         lib.dcp_partial_decode_attn.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, f32, i32,
                                                 vp, i64, i32, vp, vp, vp, sz, vp, vp]
         lib.dcp_partial_decode_attn.restype = i32
+        lib.dcp_partial_decode_attn_tokens.argtypes = lib.dcp_partial_decode_attn.argtypes
+        lib.dcp_partial_decode_attn_tokens.restype = i32
         lib.dcp_partial_decode_attn_static.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, f32,
                                                        i32, vp, i64, i32, vp, vp, vp, vp]
         lib.dcp_partial_decode_attn_static.restype = i32
@@ -157,6 +161,24 @@ def filter_page_indices(dst_vpages: torch.Tensor, n_dcp: int, d: int,
                                            _dptr(count, "count"), _stream(stream)),
            "dcp_filter_page_indices")
     return out_slot, out_src, count
+
+
+def token_reshard(seq_lens: torch.Tensor, src_page_ptr: torch.Tensor, src_pages: torch.Tensor,
+                  tok_page_ptr: torch.Tensor, tok_vpages: torch.Tensor, num_layers: int, src_pools: list,
+                  src_pool_pages: int, dst_pools: list, dst_slots_per_rank: int, dev_error: torch.Tensor | None = None,
+                  stream=None) -> None:
+    """Row gather into the token-interleaved layout (rank d holds tokens d, d + N, ...)."""
+    dtype = _kv_code(src_pools[0])
+    sp = _ptr_array(src_pools, "src_pools")
+    dp = _ptr_array(dst_pools, "dst_pools")
+    _check(_load().dcp_token_reshard(seq_lens.numel(), _dptr(seq_lens, "seq_lens", torch.int32),
+                                     _dptr(src_page_ptr, "src_page_ptr", torch.int64),
+                                     _dptr(src_pages, "src_pages", torch.int32),
+                                     _dptr(tok_page_ptr, "tok_page_ptr", torch.int64), tok_vpages.numel(),
+                                     _dptr(tok_vpages, "tok_vpages", torch.int32), dtype, num_layers, len(src_pools),
+                                     ctypes.addressof(sp), src_pool_pages, len(dst_pools), ctypes.addressof(dp),
+                                     dst_slots_per_rank, _dptr(dev_error, "dev_error", torch.int32), _stream(stream)),
+           "dcp_token_reshard")
 
 
 def naive_full_transfer(src_pages: torch.Tensor, num_layers: int, src_pools: list, src_pool_pages: int,
@@ -257,8 +279,9 @@ def partial_decode_attn(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: t
                         dst_vpages: torch.Tensor, kv_pools: list, softmax_scale: float,
                         kv_scale: float = 1.0, only_rank: int = -1, o_part: torch.Tensor | None = None,
                         lse_part: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                        dev_error: torch.Tensor | None = None, stream=None):
+                        dev_error: torch.Tensor | None = None, stream=None, layout: str = "page"):
     """Per-rank partial attention.  q: bf16 [B][T][H][576]; kv_pools: per-rank [slots][64][576].
+    layout "token": the page table is token-interleaved (dcp_partial_decode_attn_tokens).
     Returns (o_part [N][B][T][H][512] fp32, lse_part [N][B][T][H] fp32)."""
     B, T, H, kd = q.shape
     if kd != K_DIM:
@@ -278,7 +301,8 @@ def partial_decode_attn(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: t
     if workspace is None:
         workspace = alloc_workspace(B, T, H, N, num_pages, dev)
     kp = _ptr_array(kv_pools, "kv_pools")
-    _check(_load().dcp_partial_decode_attn(B, T, H, _dptr(q, "q", torch.bfloat16),
+    fn = _load().dcp_partial_decode_attn_tokens if layout == "token" else _load().dcp_partial_decode_attn
+    _check(fn(B, T, H, _dptr(q, "q", torch.bfloat16),
                                            _dptr(seq_lens, "seq_lens", torch.int32),
                                            _dptr(req_page_ptr, "req_page_ptr", torch.int64), num_pages,
                                            _dptr(dst_vpages, "dst_vpages", torch.int32), PAGE, dtype,

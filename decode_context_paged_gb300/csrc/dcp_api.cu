@@ -135,6 +135,50 @@ int dcp_reshard_pages(int num_requests, const int64_t *req_page_ptr, int64_t num
     return DCP_OK;
 }
 
+int dcp_token_reshard(int num_requests, const int32_t *seq_lens, const int64_t *src_page_ptr,
+                      const int32_t *src_pages, const int64_t *tok_page_ptr, int64_t num_tok_entries,
+                      const int32_t *tok_vpages, int dtype, int num_layers, int n_cp, const void *const *src_pools,
+                      int64_t src_pool_pages, int n_dcp, void *const *dst_pools, int64_t dst_slots_per_rank,
+                      int32_t *dev_error, dcp_stream_t stream) {
+    if (num_requests < 0 || num_tok_entries < 0 || num_layers < 0 || src_pool_pages < 0 || dst_slots_per_rank < 0)
+        return DCP_ERR_INVALID_ARG;
+    if (dtype != DCP_KV_BF16 && dtype != DCP_KV_FP8_E4M3) return DCP_ERR_INVALID_ARG;
+    if (n_cp < 1 || n_cp > kMaxCp || n_dcp < 1 || n_dcp > kMaxDcpReshard) return DCP_ERR_INVALID_ARG;
+    if (num_requests == 0 || num_tok_entries == 0 || num_layers == 0) return DCP_OK;
+    if (!seq_lens || !src_page_ptr || !src_pages || !tok_page_ptr || !tok_vpages || !src_pools || !dst_pools)
+        return DCP_ERR_INVALID_ARG;
+    TokenReshardArgs a{};
+    a.seq_lens = seq_lens;
+    a.src_page_ptr = src_page_ptr;
+    a.src_pages = src_pages;
+    a.tok_page_ptr = tok_page_ptr;
+    a.tok_vpages = tok_vpages;
+    a.num_requests = num_requests;
+    a.num_tok_entries = num_tok_entries;
+    a.row_bytes = (int64_t)kKDim * (dtype == DCP_KV_BF16 ? 2 : 1);
+    a.num_layers = num_layers;
+    a.n_cp = n_cp;
+    for (int r = 0; r < n_cp; ++r) {
+        int s0, e0;
+        layer_range(num_layers, n_cp, r, &s0, &e0);
+        a.layer_start[r] = s0;
+        a.layer_start[r + 1] = e0;
+        a.src_pools[r] = static_cast<const uint8_t *>(src_pools[r]);
+        if ((e0 > s0) && (!src_pools[r] || !aligned(src_pools[r], 16))) return DCP_ERR_INVALID_ARG;
+    }
+    a.src_pool_pages = src_pool_pages;
+    a.n_dcp = n_dcp;
+    for (int d = 0; d < n_dcp; ++d) {
+        if (!dst_pools[d] || !aligned(dst_pools[d], 16)) return DCP_ERR_INVALID_ARG;
+        a.dst_pools[d] = static_cast<uint8_t *>(dst_pools[d]);
+    }
+    a.dst_slots = dst_slots_per_rank;
+    a.dev_error = dev_error;
+    int sms = 0;
+    if (int st = current_sm_count(&sms)) return st;
+    return launch_token_reshard(a, sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? DCP_OK : DCP_ERR_CUDA;
+}
+
 int dcp_naive_full_transfer(int64_t num_pages, const int32_t *src_pages, int dtype, int num_layers, int n_cp,
                             const void *const *src_pools, int64_t src_pool_pages, int n_dcp, void *const *recv_bufs,
                             int32_t *dev_error, dcp_stream_t stream) {
@@ -268,7 +312,8 @@ static int partial_attn_impl(int num_requests, int q_len, int num_heads, const v
                             int dtype, float kv_scale, float softmax_scale, int n_dcp,
                             const void *const *kv_pools, int64_t slots_per_rank, int only_rank,
                             float *o_part, float *lse_part, float *o_out, float *lse_out, void *workspace,
-                            size_t workspace_bytes, int32_t *dev_error, dcp_stream_t stream) {
+                            size_t workspace_bytes, int32_t *dev_error, dcp_stream_t stream,
+                            int token_layout = 0) {
     if (num_requests < 0 || q_len < 1 || num_heads < 1 || num_pages < 0 || page_size != kPage)
         return DCP_ERR_INVALID_ARG;
     if (dtype != DCP_KV_BF16 && dtype != DCP_KV_FP8_E4M3) return DCP_ERR_INVALID_ARG;
@@ -302,6 +347,7 @@ static int partial_attn_impl(int num_requests, int q_len, int num_heads, const v
     a.lse_part = lse_part;
     a.o_out = o_out;
     a.lse_out = lse_out;
+    a.token_layout = token_layout;
     a.workspace = static_cast<uint8_t *>(workspace);
     a.dev_error = dev_error;
     a.wait_limit_ns = wait_limit_ns();
@@ -318,6 +364,18 @@ int dcp_partial_decode_attn(int num_requests, int q_len, int num_heads, const vo
     return partial_attn_impl(num_requests, q_len, num_heads, q, seq_lens, req_page_ptr, num_pages, dst_vpages,
                              page_size, dtype, kv_scale, softmax_scale, n_dcp, kv_pools, slots_per_rank, only_rank,
                              o_part, lse_part, nullptr, nullptr, workspace, workspace_bytes, dev_error, stream);
+}
+
+int dcp_partial_decode_attn_tokens(int num_requests, int q_len, int num_heads, const void *q,
+                                   const int32_t *seq_lens, const int64_t *req_page_ptr, int64_t num_pages,
+                                   const int32_t *dst_vpages, int page_size, int dtype, float kv_scale,
+                                   float softmax_scale, int n_dcp, const void *const *kv_pools,
+                                   int64_t slots_per_rank, int only_rank, float *o_part, float *lse_part,
+                                   void *workspace, size_t workspace_bytes, int32_t *dev_error,
+                                   dcp_stream_t stream) {
+    return partial_attn_impl(num_requests, q_len, num_heads, q, seq_lens, req_page_ptr, num_pages, dst_vpages,
+                             page_size, dtype, kv_scale, softmax_scale, n_dcp, kv_pools, slots_per_rank, only_rank,
+                             o_part, lse_part, nullptr, nullptr, workspace, workspace_bytes, dev_error, stream, 1);
 }
 
 int dcp_decode_attn_merged(int num_requests, int q_len, int num_heads, const void *q,

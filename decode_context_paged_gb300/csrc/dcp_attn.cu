@@ -145,6 +145,7 @@ struct KParams {
     int B, T, H, HB, G, R;
     long long num_pages;
     int oob_row;               // a TMA row coordinate past the pool (zero fill)
+    int tok_n;                 // 0: page-interleaved positions; N: token-interleaved with N ranks
     float sl2;                 // softmax_scale * kappa * log2(e)
     float out_scale;           // kappa (BF16) or kappa / 256 (FP8) applied to O
     float *o_part, *lse_part, *part_o, *part_lse;
@@ -726,7 +727,11 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     tc_fence_before();
                     mbar_arrive(&ctl->s_free[sb]);
                     // mask: ragged last page / missing second page / causal limit
-                    const bool valid = j_cur >= 0 && (long long)j_cur * 64 + (row & 63) <= (long long)u.limit;
+                    // position of this row: 64 j + r (page layout), or (64 (j div N) + r) N + j mod N
+                    // (token layout: entry j = jj N + d is rank d's local page jj)
+                    const long long pos = p.tok_n == 0 ? (long long)j_cur * 64 + (row & 63)
+                        : ((long long)(j_cur / p.tok_n) * 64 + (row & 63)) * p.tok_n + (j_cur % p.tok_n);
+                    const bool valid = j_cur >= 0 && pos <= (long long)u.limit;
 #pragma unroll
                     for (int c = 0; c < kCols; ++c) {
                         s[c] = valid ? s[c] * qsr[c] : -INFINITY;
@@ -1351,6 +1356,7 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     kp.R = R;
     kp.num_pages = s.num_pages;
     kp.oob_row = (int)std::min<int64_t>((int64_t)pool_rows, 0x7fffff00);
+    kp.tok_n = a.token_layout ? std::max(s.N, 1) : 0;
     const float kappa = f8 ? a.kv_scale : 1.f;
     kp.sl2 = a.softmax_scale * kappa * 1.4426950408889634f;
     kp.out_scale = f8 ? kappa / kPScale : kappa;

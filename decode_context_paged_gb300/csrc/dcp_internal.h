@@ -61,6 +61,27 @@ struct ReshardArgs {
 };
 cudaError_t launch_reshard(const ReshardArgs &a, int num_sms, cudaStream_t stream);
 
+// ---- token-interleaved reshard: a row gather into the token-interleaved layout (dcp_reshard.cu)
+struct TokenReshardArgs {
+    const int32_t *seq_lens;
+    const int64_t *src_page_ptr;   // prefill-side CSR: request b's source pages
+    const int32_t *src_pages;
+    const int64_t *tok_page_ptr;   // destination CSR: entry jj N + d = rank d's local page jj
+    const int32_t *tok_vpages;
+    int num_requests;
+    int64_t num_tok_entries;
+    int64_t row_bytes;
+    int num_layers, n_cp;
+    int layer_start[kMaxCp + 1];
+    const uint8_t *src_pools[kMaxCp];
+    int64_t src_pool_pages;
+    int n_dcp;
+    uint8_t *dst_pools[kMaxDcpReshard];
+    int64_t dst_slots;
+    int32_t *dev_error;
+};
+cudaError_t launch_token_reshard(const TokenReshardArgs &a, int num_sms, cudaStream_t stream);
+
 // ---- the naive baseline: full transfer to every DCP rank, then an in-place shard (dcp_reshard.cu)
 struct NaiveArgs {
     ReshardArgs base;                     // page table, layer split, source and destination pools
@@ -128,6 +149,7 @@ struct AttnArgs {
     float *lse_part;
     float *o_out;    // non-null: also merge the ranks' partials (exact LSE merge) into o_out / lse_out
     float *lse_out;
+    int token_layout;  // 1: the page table is token-interleaved (entry jj N + d = rank d's local page jj)
     uint8_t *workspace;
     int32_t *dev_error;
     uint64_t wait_limit_ns;

@@ -64,6 +64,61 @@ __global__ void __launch_bounds__(32, 1) reshard_kernel(const __grid_constant__ 
     copy_ring(c_begin, c_end, map, smem, a.dev_error, a.wait_limit_ns);
 }
 
+// Token-interleaved layout ("SGLang's path": rank d holds tokens d, d + N, d + 2N, ...): every
+// destination local page (layer l, entry e = jj N + d of request b) gathers its 64 rows, row i
+// being token t = (64 jj + i) N + d, from row t mod 64 of the request's source page t div 64 of
+// the CP rank that owns layer l.  One block per destination page (grid-stride), 16-byte vectors.
+constexpr int kTokThreads = 256;
+
+__global__ void __launch_bounds__(kTokThreads) token_reshard_kernel(const __grid_constant__ TokenReshardArgs a) {
+    grid_dep_wait();
+    grid_dep_launch();
+    const int n = a.n_dcp <= 1 ? 1 : a.n_dcp;
+    const int vecs = (int)(a.row_bytes / 16);
+    const int64_t page_bytes = a.row_bytes * 64;
+    const int64_t items = (int64_t)a.num_layers * a.num_tok_entries;
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+        const int l = (int)(item / a.num_tok_entries);
+        const int64_t eg = item - (int64_t)l * a.num_tok_entries;
+        int lo = 0, hi = a.num_requests;  // request b with tok_page_ptr[b] <= eg < tok_page_ptr[b + 1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (__ldg(a.tok_page_ptr + mid) <= eg) lo = mid;
+            else hi = mid;
+        }
+        const int b = lo;
+        const int64_t e = eg - __ldg(a.tok_page_ptr + b);
+        const int64_t jj = e / n;
+        const int d = (int)(e - jj * n);
+        const int32_t v = __ldg(a.tok_vpages + eg);
+        const int64_t slot = a.n_dcp <= 1 ? (int64_t)v : (int64_t)(v / a.n_dcp);
+        const int owner = a.n_dcp <= 1 ? 0 : (int)(v % a.n_dcp);
+        if (v < 0 || owner != d || slot >= a.dst_slots) {
+            if (threadIdx.x == 0 && a.dev_error) atomicOr(a.dev_error, DCP_DEVERR_OUT_OF_RANGE);
+            continue;
+        }
+        int r = 0;
+        while (r + 1 < a.n_cp && l >= a.layer_start[r + 1]) ++r;
+        const int64_t n_b = __ldg(a.seq_lens + b);
+        const int64_t sp0 = __ldg(a.src_page_ptr + b);
+        uint8_t *dst = a.dst_pools[d] + ((int64_t)l * a.dst_slots + slot) * page_bytes;
+        const uint8_t *src_layer = a.src_pools[r] + (int64_t)(l - a.layer_start[r]) * a.src_pool_pages * page_bytes;
+        for (int idx = threadIdx.x; idx < 64 * vecs; idx += blockDim.x) {
+            const int i = idx / vecs, c = idx - i * vecs;
+            const int64_t t = (64 * jj + i) * n + d;
+            if (t >= n_b) continue;
+            const int32_t sp = __ldg(a.src_pages + sp0 + t / 64);
+            if (sp < 0 || sp >= a.src_pool_pages) {
+                if (a.dev_error) atomicOr(a.dev_error, DCP_DEVERR_OUT_OF_RANGE);
+                continue;
+            }
+            const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src_layer + (int64_t)sp * page_bytes +
+                                                                  (t % 64) * a.row_bytes) + c);
+            reinterpret_cast<uint4 *>(dst + (int64_t)i * a.row_bytes)[c] = x;
+        }
+    }
+}
+
 // The pages' initial design, kept as a bandwidth baseline ("Design Evolution", 6.1).
 // Mode 0 (full transfer): every page entry of every layer to every DCP rank's receive buffer
 // [layer][page entry] (N_dcp times the KV).  Mode 1 (in-place shard): each page entry of each
@@ -225,6 +280,13 @@ cudaError_t launch_reshard(const ReshardArgs &a, int num_sms, cudaStream_t strea
                                          (int)kRingSmem);
     if (e != cudaSuccess) return e;
     return launch_pdl(reshard_kernel, dim3(num_sms), dim3(32), kRingSmem, stream, a);
+}
+
+cudaError_t launch_token_reshard(const TokenReshardArgs &a, int num_sms, cudaStream_t stream) {
+    const int64_t items = (int64_t)a.num_layers * a.num_tok_entries;
+    if (items <= 0) return cudaSuccess;
+    const int grid = (int)(items < 8LL * num_sms ? items : 8LL * num_sms);
+    return launch_pdl(token_reshard_kernel, dim3(grid), dim3(kTokThreads), 0, stream, a);
 }
 
 cudaError_t launch_naive(const NaiveArgs &a, int num_sms, cudaStream_t stream) {

@@ -133,6 +133,36 @@ int dcp_reshard_pages(int num_requests, const int64_t *req_page_ptr, int64_t num
                       int only_dst_rank, int32_t *dev_error, dcp_stream_t stream);
 
 /*
+ * [P2] token-interleaved DCP: rank d holds tokens d, d + N, d + 2N, ... of every request
+ * (N = n_dcp).  Destination table (tok_page_ptr int64 [num_requests+1], tok_vpages int32
+ * [num_tok_entries], device): entry jj * N + d of request b names rank d's local page jj by its
+ * page value v (owner v mod N must be d, slot v div N), and row i of it holds token
+ * (64 jj + i) * N + d.  The reshard from the prefill layout (request b's token t at row t mod
+ * 64 of its source page src_pages[src_page_ptr[b] + t div 64], per source rank and layer as in
+ * dcp_reshard_pages) is a row gather: for every layer l and token t < seq_lens[b],
+ *     dst_pools[t mod N][l][slot(v)][(t div N) mod 64]  <-  source row of t.
+ * Rows past seq_lens[b] are left untouched.  Entries whose value names another owner, slots or
+ * source indices outside their pools set DCP_DEVERR_OUT_OF_RANGE and are skipped.
+ * dcp_partial_decode_attn_tokens computes dcp_partial_decode_attn's partials over such a table:
+ * identical arguments, with key positions (64 jj + i) * N + d instead of 64 j + i.  The merge
+ * is unchanged (dcp_lse_merge).  The pages' own design is page-interleaved ([P1] 5.1); this
+ * layout is the alternative [P2] names.  Returns DCP_ERR_INVALID_ARG, DCP_ERR_CUDA.
+ */
+int dcp_token_reshard(int num_requests, const int32_t *seq_lens, const int64_t *src_page_ptr,
+                      const int32_t *src_pages, const int64_t *tok_page_ptr, int64_t num_tok_entries,
+                      const int32_t *tok_vpages, int dtype, int num_layers, int n_cp,
+                      const void *const *src_pools, int64_t src_pool_pages, int n_dcp,
+                      void *const *dst_pools, int64_t dst_slots_per_rank, int32_t *dev_error,
+                      dcp_stream_t stream);
+int dcp_partial_decode_attn_tokens(int num_requests, int q_len, int num_heads, const void *q,
+                                   const int32_t *seq_lens, const int64_t *req_page_ptr,
+                                   int64_t num_pages, const int32_t *dst_vpages, int page_size,
+                                   int dtype, float kv_scale, float softmax_scale, int n_dcp,
+                                   const void *const *kv_pools, int64_t slots_per_rank,
+                                   int only_rank, float *o_part, float *lse_part, void *workspace,
+                                   size_t workspace_bytes, int32_t *dev_error, dcp_stream_t stream);
+
+/*
  * [P1] 6.1 "Design Evolution", the initial design, kept as the bandwidth baseline of the 2D
  * reshard: prefill sends the full, unsharded KV to every decode DCP rank, then each rank keeps
  * the pages it owns (the in-place shard).  The two calls together leave dst_pools exactly as

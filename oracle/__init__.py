@@ -75,6 +75,10 @@ def _load():
                                            i64, i32, vp, i64, vp, vp]
             lib.dcpo_attention.restype = i32
             lib.dcpo_lse_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp]
+            lib.dcpo_attention_tokens.argtypes = lib.dcpo_attention.argtypes
+            lib.dcpo_attention_tokens.restype = i32
+            lib.dcpo_token_reshard.argtypes = [i32, vp, vp, vp, vp, vp, i64, i32, i32, vp, i64, i32, vp, i64]
+            lib.dcpo_token_reshard.restype = i32
             lib.dcpo_full_transfer.argtypes = [i64, vp, i64, i32, i32, vp, i64, i32, vp]
             lib.dcpo_full_transfer.restype = i32
             lib.dcpo_inplace_shard.argtypes = [i64, vp, i64, i32, i32, vp, vp, i64]
@@ -140,6 +144,23 @@ def reshard(req_page_ptr, src_pages, dst_vpages, page_bytes: int, n_layers: int,
                                     n_layers, len(src_pools), ctypes.addressof(sarr),
                                     src_pool_pages, n_dcp, ctypes.addressof(darr), dst_slots,
                                     only_src, only_dst))
+
+
+def token_reshard(seq_lens, src_page_ptr, src_pages, tok_page_ptr, tok_vpages, row_bytes: int, n_layers: int,
+                  src_pools: list, src_pool_pages: int, n_dcp: int, dst_pools: list, dst_slots: int) -> int:
+    """Token-interleaved reshard (row gather) into ``dst_pools`` (modified in place)."""
+    sl = _c(seq_lens, np.int32)
+    spp = _c(src_page_ptr, np.int64)
+    sp = _c(src_pages, np.int32)
+    tpp = _c(tok_page_ptr, np.int64)
+    tv = _c(tok_vpages, np.int32)
+    for p in list(src_pools) + list(dst_pools):
+        assert p.dtype == np.uint8 and p.flags["C_CONTIGUOUS"]
+    sarr = (ctypes.c_void_p * len(src_pools))(*[_ptr(p) for p in src_pools])
+    darr = (ctypes.c_void_p * len(dst_pools))(*[_ptr(p) for p in dst_pools])
+    return int(_load().dcpo_token_reshard(sl.size, _ptr(sl), _ptr(spp), _ptr(sp), _ptr(tpp), _ptr(tv), row_bytes,
+                                          n_layers, len(src_pools), ctypes.addressof(sarr), src_pool_pages, n_dcp,
+                                          ctypes.addressof(darr), dst_slots))
 
 
 def full_transfer(src_pages, page_bytes: int, n_layers: int, src_pools: list, src_pool_pages: int, n_dcp: int,
@@ -209,8 +230,10 @@ def decode_e4m3(bits) -> np.ndarray:
 
 def attention(q_bits, seq_lens, req_page_ptr, dst_vpages, kv_pools: list[np.ndarray],
               dtype: int, kv_scale: float, softmax_scale: float, n_dcp: int, rank: int = -1,
-              rows=None, q_len: int = 1, num_heads: int | None = None):
-    """Partial (rank >= 0) or unsharded (rank = -1) attention in float64.
+              rows=None, q_len: int = 1, num_heads: int | None = None, layout: str = "page"):
+    """Partial (rank >= 0) or unsharded (rank = -1) attention in float64.  layout "page": entry j
+    of a request's table holds positions 64 j + i; "token": entry jj * N + d is rank d's local page
+    jj, holding positions (64 jj + i) * N + d.
 
     q_bits: uint16 BF16 bits [B][T][H][576]; kv_pools: per-rank arrays whose raw bytes are
     [slots][64][576] BF16 (uint16) or E4M3 (uint8).  Returns (o [rows][512], lse [rows]).
@@ -236,7 +259,8 @@ def attention(q_bits, seq_lens, req_page_ptr, dst_vpages, kv_pools: list[np.ndar
         n_rows = rws.size
     o = np.zeros((n_rows, V_DIM), np.float64)
     lse = np.zeros(n_rows, np.float64)
-    st = _load().dcpo_attention(b_count, q_len, num_heads, _ptr(q), _ptr(sl), _ptr(rpp), _ptr(dv),
+    fn = _load().dcpo_attention_tokens if layout == "token" else _load().dcpo_attention
+    st = fn(b_count, q_len, num_heads, _ptr(q), _ptr(sl), _ptr(rpp), _ptr(dv),
                                 dtype, float(kv_scale), float(softmax_scale), n_dcp,
                                 ctypes.addressof(parr), slots, rank,
                                 _ptr(rws) if rws is not None else None, n_rows, _ptr(o), _ptr(lse))

@@ -217,11 +217,20 @@ static double kv_element(const void *pool, int dtype, int64_t elem_index, double
 /* Outputs are indexed by the flat row index (o: [rows][512], lse: [rows]).               */
 /* Returns 0, or -2 if a page slot is outside the pool.                                   */
 /* ------------------------------------------------------------------------------------ */
-int dcpo_attention(int num_requests, int q_len, int num_heads, const uint16_t *q,
-                   const int32_t *seq_lens, const int64_t *req_page_ptr,
-                   const int32_t *dst_vpages, int dtype, double kv_scale, double softmax_scale,
-                   int n_dcp, const void *const *kv_pools, int64_t slots_per_rank, int rank,
-                   const int64_t *rows, int64_t n_rows, double *o, double *lse) {
+/* Position of row i of table entry j of a request: 64 j + i for the page-interleaved layout
+ * ([P1] 5.1); for the token-interleaved layout ([P2]: rank d holds tokens d, d + N, d + 2N,
+ * ...), entry j = jj * N + d is rank d's local page jj and its row i holds token
+ * (64 jj + i) * N + d. */
+static int64_t key_position(int64_t j, int i, int n_dcp, int token_layout) {
+    if (!token_layout || n_dcp <= 1) return j * DCPO_PAGE_TOKENS + i;
+    return ((j / n_dcp) * DCPO_PAGE_TOKENS + i) * n_dcp + (j % n_dcp);
+}
+
+static int attention_impl(int num_requests, int q_len, int num_heads, const uint16_t *q,
+                          const int32_t *seq_lens, const int64_t *req_page_ptr,
+                          const int32_t *dst_vpages, int dtype, double kv_scale, double softmax_scale,
+                          int n_dcp, const void *const *kv_pools, int64_t slots_per_rank, int rank,
+                          const int64_t *rows, int64_t n_rows, double *o, double *lse, int token_layout) {
     int64_t all_rows = (int64_t)num_requests * q_len * num_heads;
     int64_t count = rows ? n_rows : all_rows;
     int64_t max_keys = 0;
@@ -261,7 +270,7 @@ int dcpo_attention(int num_requests, int q_len, int num_heads, const uint16_t *q
                     continue;
                 }
                 for (int i = 0; i < DCPO_PAGE_TOKENS; ++i) {
-                    int64_t pos = j * DCPO_PAGE_TOKENS + i;
+                    int64_t pos = key_position(j, i, n_dcp, token_layout);
                     if (pos > limit) continue;
                     key_pool[nk] = kv_pools[owner];
                     key_row[nk] = slot * DCPO_PAGE_TOKENS + i;
@@ -298,6 +307,66 @@ int dcpo_attention(int num_requests, int q_len, int num_heads, const uint16_t *q
         free(scores);
         free(key_pool);
         free(key_row);
+    }
+    return status;
+}
+
+int dcpo_attention(int num_requests, int q_len, int num_heads, const uint16_t *q,
+                   const int32_t *seq_lens, const int64_t *req_page_ptr,
+                   const int32_t *dst_vpages, int dtype, double kv_scale, double softmax_scale,
+                   int n_dcp, const void *const *kv_pools, int64_t slots_per_rank, int rank,
+                   const int64_t *rows, int64_t n_rows, double *o, double *lse) {
+    return attention_impl(num_requests, q_len, num_heads, q, seq_lens, req_page_ptr, dst_vpages, dtype, kv_scale,
+                          softmax_scale, n_dcp, kv_pools, slots_per_rank, rank, rows, n_rows, o, lse, 0);
+}
+
+/* The same attention over the token-interleaved layout ([P2]): the table's entry j = jj * N + d
+ * names rank d's local page jj, whose row i holds token (64 jj + i) * N + d. */
+int dcpo_attention_tokens(int num_requests, int q_len, int num_heads, const uint16_t *q,
+                          const int32_t *seq_lens, const int64_t *req_page_ptr,
+                          const int32_t *dst_vpages, int dtype, double kv_scale, double softmax_scale,
+                          int n_dcp, const void *const *kv_pools, int64_t slots_per_rank, int rank,
+                          const int64_t *rows, int64_t n_rows, double *o, double *lse) {
+    return attention_impl(num_requests, q_len, num_heads, q, seq_lens, req_page_ptr, dst_vpages, dtype, kv_scale,
+                          softmax_scale, n_dcp, kv_pools, slots_per_rank, rank, rows, n_rows, o, lse, 1);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* [P2] token-interleaved DCP: rank d holds tokens d, d + N, d + 2N, ...; its local token   */
+/* q = t div N sits at row q mod 64 of its local page q div 64, named by the destination    */
+/* table's entry (q div 64) * N + d of the request.  The move from the prefill layout (token */
+/* t at row t mod 64 of source page t div 64) is a row gather, for every layer of the        */
+/* source rank that owns it ([P1] 4.1).  Rows past the sequence are left untouched.          */
+/* ------------------------------------------------------------------------------------ */
+int dcpo_token_reshard(int num_requests, const int32_t *seq_lens, const int64_t *src_page_ptr,
+                       const int32_t *src_pages, const int64_t *tok_page_ptr, const int32_t *tok_vpages,
+                       int64_t row_bytes, int n_layers, int n_cp, uint8_t *const *src_pools, int64_t src_pool_pages,
+                       int n_dcp, uint8_t *const *dst_pools, int64_t dst_slots) {
+    int status = 0;
+    int n = n_dcp <= 1 ? 1 : n_dcp;
+    int64_t page_bytes = row_bytes * DCPO_PAGE_TOKENS;
+    for (int r = 0; r < n_cp; ++r) {
+        int l0, l1;
+        dcpo_layer_range(n_layers, n_cp, r, &l0, &l1);
+        for (int l = l0; l < l1; ++l)
+            for (int b = 0; b < num_requests; ++b)
+                for (int64_t t = 0; t < seq_lens[b]; ++t) {
+                    int d = (int)(t % n);
+                    int64_t qd = t / n;
+                    int64_t e = tok_page_ptr[b] + (qd / DCPO_PAGE_TOKENS) * n + d;
+                    int32_t v = tok_vpages[e];
+                    int32_t sp = src_pages[src_page_ptr[b] + t / DCPO_PAGE_TOKENS];
+                    if (v < 0 || page_owner(v, n_dcp) != d || page_slot(v, n_dcp) >= dst_slots || sp < 0 ||
+                        sp >= src_pool_pages) {
+                        status = -2;
+                        continue;
+                    }
+                    memcpy(dst_pools[d] + ((int64_t)l * dst_slots + page_slot(v, n_dcp)) * page_bytes +
+                               (qd % DCPO_PAGE_TOKENS) * row_bytes,
+                           src_pools[r] + ((int64_t)(l - l0) * src_pool_pages + sp) * page_bytes +
+                               (t % DCPO_PAGE_TOKENS) * row_bytes,
+                           (size_t)row_bytes);
+                }
     }
     return status;
 }

@@ -337,6 +337,126 @@ def _table_for(c, n_dcp):
     return vp.numpy()
 
 
+# ------------------------------------------------------------------- token-interleaved layout
+def _dense_layouts(lens, n_dcp, H=3, T=2, seed=3):
+    """One dense BF16 token sequence per request, laid out page-interleaved ([P1] 5.1: token t
+    at row t mod 64 of entry t div 64) and token-interleaved ([P2]: rank t mod N, local token
+    t div N), with the same queries."""
+    page = di.attention_case(lens, H=H, T=T, n_dcp=n_dcp, dtype="bf16", slots_per_rank=None, seed=seed,
+                             device="cpu")
+    tok = di.token_attention_case(lens, H=H, T=T, n_dcp=n_dcp, dtype="bf16", seed=seed + 1, device="cpu")
+    tok.q = page.q.clone()
+    n_r = max(n_dcp, 1)
+    g = torch.Generator().manual_seed(seed + 7)
+    for b, n in enumerate(lens):
+        dense = torch.randn((n, 576), generator=g).to(torch.bfloat16)
+        pp, pv = page.req_page_ptr.numpy(), page.dst_vpages.numpy()
+        tp, tv = tok.req_page_ptr.numpy(), tok.dst_vpages.numpy()
+        for t in range(n):
+            v = int(pv[pp[b] + t // 64])
+            page.pools[v % n_r if n_dcp > 1 else 0][v // n_r if n_dcp > 1 else v, t % 64] = dense[t]
+            d, qd = t % n_r, t // n_r
+            w = int(tv[tp[b] + (qd // 64) * n_r + d])
+            tok.pools[d][w // n_r if n_dcp > 1 else w, qd % 64] = dense[t]
+    return page, tok
+
+
+def _call_layout(case, rank=-1):
+    q_bits, raw, _ = _np_case(case)
+    return oracle.attention(q_bits, case.seq_lens.numpy(), case.req_page_ptr.numpy(), case.dst_vpages.numpy(), raw,
+                            oracle.BF16, 1.0, case.softmax_scale, case.n_dcp, rank=rank, q_len=case.T,
+                            num_heads=case.H, layout=case.layout)
+
+
+@pytest.mark.parametrize("lens,n_dcp", [([130, 70, 5], 3), ([64 * 9 + 1], 4), ([200], 1)])
+def test_token_layout_attention_equals_page_layout_and_merges_exactly(lens, n_dcp):
+    """[P2]: with rank i holding tokens i, i + N, ..., the unsharded attention equals the
+    page-interleaved layout's over the same token sequence (both are the dense attention), and
+    the merge of the per-rank partials is exact (the LSE recombination)."""
+    page, tok = _dense_layouts(lens, n_dcp)
+    o_p, l_p = _call_layout(page)
+    o_t, l_t = _call_layout(tok)
+    np.testing.assert_allclose(o_t, o_p, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l_t, l_p, rtol=0, atol=1e-12)
+    parts = [_call_layout(tok, rank=d) for d in range(max(n_dcp, 1))]
+    o_m, l_m = oracle.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
+    np.testing.assert_allclose(o_m, o_p, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(l_m, l_p, rtol=0, atol=1e-12)
+
+
+def test_token_layout_rank_partial_brute_force():
+    """Rank d's partial covers exactly the tokens t = d mod N with t <= n - T + q (scipy)."""
+    lens, n_dcp, H, T = [150, 67], 3, 2, 2
+    page, tok = _dense_layouts(lens, n_dcp, H=H, T=T, seed=5)
+    q_bits, raw, dec = _np_case(page)
+    for d in range(n_dcp):
+        o, l = _call_layout(tok, rank=d)
+        for b, n in enumerate(lens):
+            pp, pv = page.req_page_ptr.numpy(), page.dst_vpages.numpy()
+            keys = []
+            for tt in range(n):
+                v = int(pv[pp[b] + tt // 64])
+                keys.append(dec[v % n_dcp][v // n_dcp, tt % 64])
+            keys = np.stack(keys)
+            for t in range(T):
+                for h in range(H):
+                    row = (b * T + t) * H + h
+                    vis = [tt for tt in range(n) if tt % n_dcp == d and tt <= n - T + t]
+                    qv = torch.from_numpy(q_bits[b, t, h].view(np.int16)).view(torch.bfloat16).double().numpy()
+                    if not vis:
+                        assert np.isneginf(l[row]) and not o[row].any()
+                        continue
+                    sc = page.softmax_scale * (keys[vis] @ qv)
+                    assert l[row] == pytest.approx(logsumexp(sc), abs=1e-10)
+                    np.testing.assert_allclose(o[row], softmax(sc) @ keys[vis][:, :512], rtol=0, atol=1e-10)
+
+
+def test_token_reshard_puts_token_t_at_rank_t_mod_n():
+    """[P2] layout from the prefill pages: token t of layer l lands at rank t mod N, local token
+    t div N (row (t div N) mod 64 of the page named by entry ((t div N) div 64) N + t mod N); rows
+    past the sequence keep the sentinel; layers come from their owning CP rank ([P1] 4.1)."""
+    rng = np.random.default_rng(2)
+    lens, n_dcp, n_layers, n_cp = [130, 64, 3], 3, 3, 2
+    ranges = [oracle.layer_range(n_layers, n_cp, r) for r in range(n_cp)]
+    pages = [(n + 63) // 64 for n in lens]
+    sptr = np.concatenate([[0], np.cumsum(pages)]).astype(np.int64)
+    src_pool_pages = sum(pages) + 2
+    src_pages = rng.permutation(src_pool_pages)[:sum(pages)].astype(np.int32)
+    row_bytes = 16
+    pb = 64 * row_bytes
+    src = []
+    for r, (l0, l1) in enumerate(ranges):
+        p = np.zeros(((l1 - l0), src_pool_pages, 64, row_bytes), np.uint8)
+        for l in range(l1 - l0):
+            for s in range(src_pool_pages):
+                for i in range(64):
+                    p[l, s, i, :8] = np.frombuffer(np.array([r, l, s, i], np.int16).tobytes(), np.uint8)
+        src.append(p.reshape(-1))
+    slots = 8
+    tptr, tv = di.token_page_table(lens, n_dcp, slots, torch.Generator().manual_seed(1))
+    tptr, tv = tptr.numpy(), tv.numpy()
+    dst = [np.full(n_layers * slots * pb, di.SENTINEL_BYTE, np.uint8) for _ in range(n_dcp)]
+    assert oracle.token_reshard(lens, sptr, src_pages, tptr, tv, row_bytes, n_layers, src, src_pool_pages, n_dcp,
+                                dst, slots) == 0
+    hit = set()
+    for l in range(n_layers):
+        r = next(i for i, (s0, e0) in enumerate(ranges) if s0 <= l < e0)
+        for b, n in enumerate(lens):
+            for t in range(n):
+                d, qd = t % n_dcp, t // n_dcp
+                w = int(tv[tptr[b] + (qd // 64) * n_dcp + d])
+                assert w % n_dcp == d
+                off = ((l * slots + w // n_dcp) * 64 + qd % 64) * row_bytes
+                tag = list(np.frombuffer(dst[d][off:off + 8].tobytes(), np.int16))
+                assert tag == [r, l - ranges[r][0], src_pages[sptr[b] + t // 64], t % 64]
+                hit.add((d, off))
+    for d in range(n_dcp):
+        rows = dst[d].reshape(-1, row_bytes)
+        for k in range(rows.shape[0]):
+            if (d, k * row_bytes) not in hit:
+                assert (rows[k] == di.SENTINEL_BYTE).all()
+
+
 # ------------------------------------------------------------------------------- decoders
 def test_bf16_decode_matches_format_and_torch():
     """BF16 = upper half of binary32: known encodings, and all 65536 codes vs torch's cast."""
