@@ -77,12 +77,18 @@ def _load():
         lib.dcp_partial_decode_attn.restype = i32
         lib.dcp_partial_decode_attn_tokens.argtypes = lib.dcp_partial_decode_attn.argtypes
         lib.dcp_partial_decode_attn_tokens.restype = i32
+        lib.dcp_partial_decode_attn_run.argtypes = lib.dcp_partial_decode_attn.argtypes
+        lib.dcp_partial_decode_attn_run.restype = i32
+        lib.dcp_attn_plan.argtypes = [i32, i32, i32, vp, i64, vp, i32, i32, i64, i32, vp, sz, vp, vp]
+        lib.dcp_attn_plan.restype = i32
         lib.dcp_partial_decode_attn_static.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, f32,
                                                        i32, vp, i64, i32, vp, vp, vp, vp]
         lib.dcp_partial_decode_attn_static.restype = i32
         lib.dcp_decode_attn_merged.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, f32, i32, vp,
                                                i64, vp, vp, vp, vp, vp, sz, vp, vp]
         lib.dcp_decode_attn_merged.restype = i32
+        lib.dcp_decode_attn_merged_run.argtypes = lib.dcp_decode_attn_merged.argtypes
+        lib.dcp_decode_attn_merged_run.restype = i32
         lib.dcp_lse_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp, vp]
         lib.dcp_lse_merge.restype = i32
         _lib = lib
@@ -279,9 +285,11 @@ def partial_decode_attn(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: t
                         dst_vpages: torch.Tensor, kv_pools: list, softmax_scale: float,
                         kv_scale: float = 1.0, only_rank: int = -1, o_part: torch.Tensor | None = None,
                         lse_part: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-                        dev_error: torch.Tensor | None = None, stream=None, layout: str = "page"):
+                        dev_error: torch.Tensor | None = None, stream=None, layout: str = "page",
+                        planned: bool = False):
     """Per-rank partial attention.  q: bf16 [B][T][H][576]; kv_pools: per-rank [slots][64][576].
     layout "token": the page table is token-interleaved (dcp_partial_decode_attn_tokens).
+    planned: run the plan attn_plan stored in ``workspace`` (dcp_partial_decode_attn_run).
     Returns (o_part [N][B][T][H][512] fp32, lse_part [N][B][T][H] fp32)."""
     B, T, H, kd = q.shape
     if kd != K_DIM:
@@ -301,7 +309,10 @@ def partial_decode_attn(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: t
     if workspace is None:
         workspace = alloc_workspace(B, T, H, N, num_pages, dev)
     kp = _ptr_array(kv_pools, "kv_pools")
-    fn = _load().dcp_partial_decode_attn_tokens if layout == "token" else _load().dcp_partial_decode_attn
+    if planned and (workspace is None or layout == "token"):
+        raise ValueError("a planned run needs the workspace holding the plan (page layout)")
+    fn = (_load().dcp_partial_decode_attn_run if planned else
+          _load().dcp_partial_decode_attn_tokens if layout == "token" else _load().dcp_partial_decode_attn)
     _check(fn(B, T, H, _dptr(q, "q", torch.bfloat16),
                                            _dptr(seq_lens, "seq_lens", torch.int32),
                                            _dptr(req_page_ptr, "req_page_ptr", torch.int64), num_pages,
@@ -315,12 +326,26 @@ def partial_decode_attn(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: t
     return o_part, lse_part
 
 
+def attn_plan(q_shape: tuple, req_page_ptr: torch.Tensor, dst_vpages: torch.Tensor, kv_pools: list,
+              workspace: torch.Tensor, only_rank: int = -1, dev_error: torch.Tensor | None = None, stream=None) -> None:
+    """The attention's plan for this page table into ``workspace`` (dcp_attn_plan); q_shape =
+    (B, T, H); kv_pools give the DCP size, slots per rank and dtype."""
+    B, T, H = q_shape[:3]
+    _check(_load().dcp_attn_plan(B, T, H, _dptr(req_page_ptr, "req_page_ptr", torch.int64), dst_vpages.numel(),
+                                 _dptr(dst_vpages, "dst_vpages", torch.int32), _kv_code(kv_pools[0]), len(kv_pools),
+                                 kv_pools[0].shape[0], only_rank, _dptr(workspace, "workspace"), workspace.numel(),
+                                 _dptr(dev_error, "dev_error", torch.int32), _stream(stream)),
+           "dcp_attn_plan")
+
+
 def decode_attn_merged(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: torch.Tensor,
                        dst_vpages: torch.Tensor, kv_pools: list, softmax_scale: float, kv_scale: float = 1.0,
                        o_part: torch.Tensor | None = None, lse_part: torch.Tensor | None = None,
                        o_out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None,
-                       workspace: torch.Tensor | None = None, dev_error: torch.Tensor | None = None, stream=None):
-    """Every rank's partial attention plus their exact LSE merge in one call.
+                       workspace: torch.Tensor | None = None, dev_error: torch.Tensor | None = None, stream=None,
+                       planned: bool = False):
+    """Every rank's partial attention plus their exact LSE merge in one call (planned: run the
+    plan attn_plan stored in ``workspace``, dcp_decode_attn_merged_run).
     Returns (o_out [B][T][H][512], lse_out [B][T][H], o_part, lse_part), all fp32."""
     B, T, H, kd = q.shape
     if kd != K_DIM:
@@ -344,7 +369,10 @@ def decode_attn_merged(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: to
     if workspace is None:
         workspace = alloc_workspace(B, T, H, N, num_pages, dev)
     kp = _ptr_array(kv_pools, "kv_pools")
-    _check(_load().dcp_decode_attn_merged(B, T, H, _dptr(q, "q", torch.bfloat16),
+    if planned and workspace is None:
+        raise ValueError("a planned run needs the workspace holding the plan")
+    fn = _load().dcp_decode_attn_merged_run if planned else _load().dcp_decode_attn_merged
+    _check(fn(B, T, H, _dptr(q, "q", torch.bfloat16),
                                           _dptr(seq_lens, "seq_lens", torch.int32),
                                           _dptr(req_page_ptr, "req_page_ptr", torch.int64), num_pages,
                                           _dptr(dst_vpages, "dst_vpages", torch.int32), PAGE, dtype,

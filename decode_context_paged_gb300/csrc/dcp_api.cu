@@ -313,7 +313,7 @@ static int partial_attn_impl(int num_requests, int q_len, int num_heads, const v
                             const void *const *kv_pools, int64_t slots_per_rank, int only_rank,
                             float *o_part, float *lse_part, float *o_out, float *lse_out, void *workspace,
                             size_t workspace_bytes, int32_t *dev_error, dcp_stream_t stream,
-                            int token_layout = 0) {
+                            int token_layout = 0, int phase = 0) {
     if (num_requests < 0 || q_len < 1 || num_heads < 1 || num_pages < 0 || page_size != kPage)
         return DCP_ERR_INVALID_ARG;
     if (dtype != DCP_KV_BF16 && dtype != DCP_KV_FP8_E4M3) return DCP_ERR_INVALID_ARG;
@@ -348,6 +348,7 @@ static int partial_attn_impl(int num_requests, int q_len, int num_heads, const v
     a.o_out = o_out;
     a.lse_out = lse_out;
     a.token_layout = token_layout;
+    a.phase = phase;
     a.workspace = static_cast<uint8_t *>(workspace);
     a.dev_error = dev_error;
     a.wait_limit_ns = wait_limit_ns();
@@ -376,6 +377,44 @@ int dcp_partial_decode_attn_tokens(int num_requests, int q_len, int num_heads, c
     return partial_attn_impl(num_requests, q_len, num_heads, q, seq_lens, req_page_ptr, num_pages, dst_vpages,
                              page_size, dtype, kv_scale, softmax_scale, n_dcp, kv_pools, slots_per_rank, only_rank,
                              o_part, lse_part, nullptr, nullptr, workspace, workspace_bytes, dev_error, stream, 1);
+}
+
+int dcp_attn_plan(int num_requests, int q_len, int num_heads, const int64_t *req_page_ptr, int64_t num_pages,
+                  const int32_t *dst_vpages, int dtype, int n_dcp, int64_t slots_per_rank, int only_rank,
+                  void *workspace, size_t workspace_bytes, int32_t *dev_error, dcp_stream_t stream) {
+    // The plan reads neither Q nor the pools: placeholders that pass the argument checks.
+    static const uint8_t dummy[16] __attribute__((aligned(16))) = {};
+    const void *pools[kMaxDcpAttn];
+    for (int d = 0; d < kMaxDcpAttn; ++d) pools[d] = dummy;
+    if (num_requests > 0 && !req_page_ptr) return DCP_ERR_INVALID_ARG;
+    return partial_attn_impl(num_requests, q_len, num_heads, dummy, reinterpret_cast<const int32_t *>(dummy),
+                             req_page_ptr, num_pages, dst_vpages, kPage, dtype, 1.f, 1.f, n_dcp, pools, slots_per_rank,
+                             only_rank, reinterpret_cast<float *>(const_cast<uint8_t *>(dummy)),
+                             reinterpret_cast<float *>(const_cast<uint8_t *>(dummy)), nullptr, nullptr, workspace,
+                             workspace_bytes, dev_error, stream, 0, 1);
+}
+
+int dcp_partial_decode_attn_run(int num_requests, int q_len, int num_heads, const void *q, const int32_t *seq_lens,
+                                const int64_t *req_page_ptr, int64_t num_pages, const int32_t *dst_vpages,
+                                int page_size, int dtype, float kv_scale, float softmax_scale, int n_dcp,
+                                const void *const *kv_pools, int64_t slots_per_rank, int only_rank, float *o_part,
+                                float *lse_part, void *workspace, size_t workspace_bytes, int32_t *dev_error,
+                                dcp_stream_t stream) {
+    return partial_attn_impl(num_requests, q_len, num_heads, q, seq_lens, req_page_ptr, num_pages, dst_vpages,
+                             page_size, dtype, kv_scale, softmax_scale, n_dcp, kv_pools, slots_per_rank, only_rank,
+                             o_part, lse_part, nullptr, nullptr, workspace, workspace_bytes, dev_error, stream, 0, 2);
+}
+
+int dcp_decode_attn_merged_run(int num_requests, int q_len, int num_heads, const void *q, const int32_t *seq_lens,
+                               const int64_t *req_page_ptr, int64_t num_pages, const int32_t *dst_vpages,
+                               int page_size, int dtype, float kv_scale, float softmax_scale, int n_dcp,
+                               const void *const *kv_pools, int64_t slots_per_rank, float *o_part, float *lse_part,
+                               float *o_out, float *lse_out, void *workspace, size_t workspace_bytes,
+                               int32_t *dev_error, dcp_stream_t stream) {
+    if (num_requests > 0 && (!o_out || !lse_out || !aligned(o_out, 16))) return DCP_ERR_INVALID_ARG;
+    return partial_attn_impl(num_requests, q_len, num_heads, q, seq_lens, req_page_ptr, num_pages, dst_vpages,
+                             page_size, dtype, kv_scale, softmax_scale, n_dcp, kv_pools, slots_per_rank, -1, o_part,
+                             lse_part, o_out, lse_out, workspace, workspace_bytes, dev_error, stream, 0, 2);
 }
 
 int dcp_decode_attn_merged(int num_requests, int q_len, int num_heads, const void *q,

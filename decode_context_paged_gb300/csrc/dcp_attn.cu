@@ -1111,12 +1111,13 @@ plan_build_kernel(int B, int N, int G, int only_rank, int tpc, long long num_pag
 
 // Merge the chunk partials of the multi-chunk (rank, request) pairs listed by the plan into
 // O_part / LSE_part; a grid-stride loop over (listed pair, query group, row), one warp each.
-__global__ void combine_kernel(int B, int T, int H, int HB, int G, const int *__restrict__ ctrl,
+__global__ void combine_kernel(int B, int T, int H, int HB, int G, int *ctrl,
                                const int32_t *__restrict__ multi_list, const int32_t *__restrict__ pair_chunks,
                                const int32_t *__restrict__ pair_part, const float *part_o, const float *part_lse,
                                float *o_part, float *lse_part) {
     grid_dep_wait();
     grid_dep_launch();
+    if (blockIdx.x == 0 && threadIdx.x == 0) ctrl[1] = 0;  // the work counter, ready for the next run of the plan
     const long long n_tasks = (long long)ctrl[2] * G * kGroupRows;
     const int wpb = blockDim.x >> 5;
     for (long long task = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); task < n_tasks;
@@ -1141,13 +1142,14 @@ __global__ void combine_kernel(int B, int T, int H, int HB, int G, const int *__
 // Fused merge, first launch after the attention kernel.  With no multi-chunk pair (ctrl[2] ==
 // 0) it merges every row over the ranks, one warp per row, ascending rank order.  Otherwise it combines the chunk partials as combine_kernel does
 // and leaves the rank merge to merge_after_combine_kernel.
-__global__ void merge_combine_kernel(int B, int T, int H, int HB, int G, int N, const int *__restrict__ ctrl,
+__global__ void merge_combine_kernel(int B, int T, int H, int HB, int G, int N, int *ctrl,
                                      const int32_t *__restrict__ multi_list, const int32_t *__restrict__ pair_chunks,
                                      const int32_t *__restrict__ pair_part, const float *part_o,
                                      const float *part_lse, float *o_part, float *lse_part, float *o_out,
                                      float *lse_out) {
     grid_dep_wait();
     grid_dep_launch();
+    if (blockIdx.x == 0 && threadIdx.x == 0) ctrl[1] = 0;  // the work counter, ready for the next run of the plan
     const int n_multi = ctrl[2];
     const int wpb = blockDim.x >> 5;
     if (n_multi > 0) {
@@ -1312,17 +1314,21 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     // blocks per request: about three blocks per SM in all, at most one per tile
     const int tile_stride = (int)std::max<long long>(
         1, std::min<long long>(s.tiles_per_req, (3LL * num_sms + s.B - 1) / s.B));
-    const int n_tile_blocks = s.B * tile_stride;
-    const int q_blocks = f8 ? (R + kPlanThreads / 32 - 1) / (kPlanThreads / 32) : 0;
-    if (launch_pdl(plan_count_kernel, dim3(n_tile_blocks + q_blocks), dim3(kPlanThreads), 0, stream, s.N,
+    // the plan (page-table work) unless running a stored plan; the FP8 Q split unless planning only
+    const int n_tile_blocks = a.phase == 2 ? 0 : s.B * tile_stride;
+    const int q_blocks = (f8 && a.phase != 1) ? (R + kPlanThreads / 32 - 1) / (kPlanThreads / 32) : 0;
+    if (n_tile_blocks + q_blocks > 0 &&
+        launch_pdl(plan_count_kernel, dim3(n_tile_blocks + q_blocks), dim3(kPlanThreads), 0, stream, s.N,
                    (long long)a.slots_per_rank, s.tiles_per_req, tile_stride, n_tile_blocks, a.req_page_ptr, a.dst_vpages, tile_cnt,
                    a.dev_error, R, reinterpret_cast<const __nv_bfloat16 *>(a.q), qhl, qscale) != cudaSuccess)
         return DCP_ERR_CUDA;
-    if (launch_pdl(plan_build_kernel, dim3(n_tile_blocks + 1), dim3(kPlanThreads), 0, stream, s.B, s.N, s.G,
+    if (a.phase != 2 &&
+        launch_pdl(plan_build_kernel, dim3(n_tile_blocks + 1), dim3(kPlanThreads), 0, stream, s.B, s.N, s.G,
                    a.only_rank, s.tiles_per_chunk, (long long)s.num_pages, (long long)a.slots_per_rank, s.tiles_per_req,
                    tile_stride, a.req_page_ptr, a.dst_vpages, (const int32_t *)tile_cnt, comp_slot, comp_page, counts, pair_chunks,
                    pair_part, multi_list, units, ctrl) != cudaSuccess)
         return DCP_ERR_CUDA;
+    if (a.phase == 1) return DCP_OK;
 
     AttnMaps maps;
     memset(&maps, 0, sizeof(maps));
@@ -1374,7 +1380,7 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
         const long long tasks = std::max<long long>(rows, (long long)s.N * s.B * s.G * kGroupRows);
         const int blocks = (int)std::max<long long>(1, std::min<long long>((tasks + 7) / 8, 8LL * num_sms));
         if (launch_pdl(merge_combine_kernel, dim3(blocks), dim3(256), 0, stream, s.B, s.T, s.H, kp.HB, s.G, s.N,
-                       (const int *)ctrl, (const int32_t *)multi_list, (const int32_t *)pair_chunks,
+                       ctrl, (const int32_t *)multi_list, (const int32_t *)pair_chunks,
                        (const int32_t *)pair_part, (const float *)part_o, (const float *)part_lse, a.o_part,
                        a.lse_part, a.o_out, a.lse_out) != cudaSuccess)
             return DCP_ERR_CUDA;
@@ -1389,7 +1395,7 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     const long long max_tasks = (long long)s.N * s.B * s.G * kGroupRows;
     const int combine_blocks = (int)std::max<long long>(1, std::min<long long>((max_tasks + 7) / 8, 8LL * num_sms));
     if (launch_pdl(combine_kernel, dim3(combine_blocks), dim3(256), 0, stream, s.B, s.T, s.H, kp.HB, s.G,
-                   (const int *)ctrl, (const int32_t *)multi_list, (const int32_t *)pair_chunks,
+                   ctrl, (const int32_t *)multi_list, (const int32_t *)pair_chunks,
                    (const int32_t *)pair_part, (const float *)part_o, (const float *)part_lse, a.o_part,
                    a.lse_part) != cudaSuccess)
         return DCP_ERR_CUDA;

@@ -150,6 +150,7 @@ struct AttnArgs {
     float *o_out;    // non-null: also merge the ranks' partials (exact LSE merge) into o_out / lse_out
     float *lse_out;
     int token_layout;  // 1: the page table is token-interleaved (entry jj N + d = rank d's local page jj)
+    int phase;         // 0: plan and run; 1: plan only (page-table work into the workspace); 2: run a plan
     uint8_t *workspace;
     int32_t *dev_error;
     uint64_t wait_limit_ns;

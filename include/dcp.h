@@ -280,6 +280,38 @@ int dcp_decode_attn_merged(int num_requests, int q_len, int num_heads, const voi
                            int32_t *dev_error, dcp_stream_t stream);
 
 /*
+ * Plan once, run per layer.  The attention's plan (per-rank page compaction, chunks, unit list)
+ * depends only on the page table, the sizes and the KV dtype, which every layer of a decode step
+ * shares (and which are known before the KV transfer ends).  dcp_attn_plan writes it into the
+ * workspace; dcp_partial_decode_attn_run / dcp_decode_attn_merged_run then compute exactly what
+ * dcp_partial_decode_attn / dcp_decode_attn_merged compute, without the plan launches, for any
+ * number of runs (each run leaves the plan ready for the next).  Runs must use the same
+ * num_requests, q_len, num_heads, page table (req_page_ptr, num_pages, dst_vpages), dtype,
+ * n_dcp, slots_per_rank and only_rank as the plan, and the same workspace; q, seq_lens (with
+ * the same page counts), pools and scales may differ per run.  Nothing checks that the
+ * workspace holds a matching plan.  Calls on one workspace must not overlap on the GPU.
+ * Returns the statuses of dcp_partial_decode_attn.
+ */
+int dcp_attn_plan(int num_requests, int q_len, int num_heads, const int64_t *req_page_ptr,
+                  int64_t num_pages, const int32_t *dst_vpages, int dtype, int n_dcp,
+                  int64_t slots_per_rank, int only_rank, void *workspace, size_t workspace_bytes,
+                  int32_t *dev_error, dcp_stream_t stream);
+int dcp_partial_decode_attn_run(int num_requests, int q_len, int num_heads, const void *q,
+                                const int32_t *seq_lens, const int64_t *req_page_ptr,
+                                int64_t num_pages, const int32_t *dst_vpages, int page_size,
+                                int dtype, float kv_scale, float softmax_scale, int n_dcp,
+                                const void *const *kv_pools, int64_t slots_per_rank,
+                                int only_rank, float *o_part, float *lse_part, void *workspace,
+                                size_t workspace_bytes, int32_t *dev_error, dcp_stream_t stream);
+int dcp_decode_attn_merged_run(int num_requests, int q_len, int num_heads, const void *q,
+                               const int32_t *seq_lens, const int64_t *req_page_ptr,
+                               int64_t num_pages, const int32_t *dst_vpages, int page_size,
+                               int dtype, float kv_scale, float softmax_scale, int n_dcp,
+                               const void *const *kv_pools, int64_t slots_per_rank, float *o_part,
+                               float *lse_part, float *o_out, float *lse_out, void *workspace,
+                               size_t workspace_bytes, int32_t *dev_error, dcp_stream_t stream);
+
+/*
  * Partial attention for callers that cannot allocate device memory.  The pages have no
  * counterpart to this entry point; it exists for callers that cannot call cudaMalloc, such
  * as a host whose pool allocator owns all device memory and hands plug-ins only tensor
