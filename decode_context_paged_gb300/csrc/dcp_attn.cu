@@ -68,6 +68,12 @@ constexpr float kPScale = 4.f;           // FP8 P is stored as 4 * p (p <= 2^6 u
 // this long stays far below the output tolerance, while short segments keep the lo term.
 constexpr int kSinglePMinPages = 128;
 
+#ifndef DCP_ATTN_S_BUFS_BF16
+#define DCP_ATTN_S_BUFS_BF16 3
+#endif
+#ifndef DCP_ATTN_S_BUFS_F8
+#define DCP_ATTN_S_BUFS_F8 2
+#endif
 #ifndef DCP_ATTN_K_SLOTS_BF16
 #define DCP_ATTN_K_SLOTS_BF16 4
 #endif
@@ -95,7 +101,7 @@ struct Cfg {
     static constexpr int kKBlocks = F8 ? 5 : 9;     // K-stream blocks per tile
     static constexpr int kVUnits = F8 ? 2 : 4;      // V-stream units per tile
     static constexpr int kSCols = F8 ? 128 : 64;    // TMEM columns per S buffer (hi, lo for FP8)
-    static constexpr int kSBufs = F8 ? 2 : 3;
+    static constexpr int kSBufs = F8 ? DCP_ATTN_S_BUFS_F8 : DCP_ATTN_S_BUFS_BF16;
     static constexpr uint32_t kIdescS = F8 ? idesc_e4m3_f32(128, 128, 0, 0) : idesc_bf16_f32(128, 64, 0, 0);
     static constexpr uint32_t kIdescPV = F8 ? idesc_e4m3_f32(128, 64, 1, 1) : idesc_bf16_f32(128, 64, 1, 1);
 };
