@@ -153,6 +153,11 @@ ATTN_CASES = [
     ("heads-96-fp8", [700, 333], 96, 1, 3, "e4m3"),
     # one long segment per rank (single-term FP8 P) next to short ones (hi + lo P)
     ("mixed-len-fp8", [70_000, 9_000], 64, 1, 8, "e4m3"),
+    # the largest DCP size, 32 heads (half a query group), 128 heads (two groups) with q_len 2
+    ("dcp16", [5000, 700, 1], 64, 1, 16, "bf16"),
+    ("dcp16-fp8", [5000, 70], 64, 1, 16, "e4m3"),
+    ("heads-32", [900, 64], 32, 1, 4, "bf16"),
+    ("heads-128-q2-fp8", [1200, 300], 128, 2, 4, "e4m3"),
 ]
 
 
@@ -232,3 +237,16 @@ def test_attention_long_eagle_full_size_sampled(cuda_device):
     """4 x 1,048,576 tokens, q_len 4 causal, FP8, DCP=8; sampled rows incl. every new token."""
     case = di.long_eagle_case(cuda_device)
     _sampled(case, *_run_attention(case), n_rows=12, ranks=(3,))
+
+
+def test_attention_and_merge_with_no_requests(cuda_device):
+    """An empty batch is a no-op (no launch, no error)."""
+    case = di.attention_case([64], H=64, T=1, n_dcp=2, dtype="bf16", slots_per_rank=None, seed=1,
+                             device=cuda_device)
+    q = case.q[:0]
+    seq = case.seq_lens[:0]
+    ptr = case.req_page_ptr[:1]
+    o, l = dcp.partial_decode_attn(q, seq, ptr, case.dst_vpages[:0], case.pools, case.softmax_scale)
+    om, lm, _, _ = dcp.decode_attn_merged(q, seq, ptr, case.dst_vpages[:0], case.pools, case.softmax_scale)
+    torch.cuda.synchronize()
+    assert o.numel() == 0 and om.numel() == 0 and lm.numel() == 0
