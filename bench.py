@@ -39,9 +39,9 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # on; a changed source reports traffic null until it is re-measured.
 NCU_TRAFFIC = {
     # (kernel, workload): (source hash, DRAM bytes per launch)
-    ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("a1469b33d4862d63", 552190720),
-    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("beefb70bb5b40fc3", 328204544),
-    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("beefb70bb5b40fc3", 3068986136),
+    ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("291728be04d95f89", 552155136),
+    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("68f9b5162613d53d", 327527168),
+    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("68f9b5162613d53d", 3068039480),
 }
 
 
