@@ -15,7 +15,13 @@
  *   dcp_partial_decode_attn  -- paged absorbed-MLA decode attention per rank ([P1] 5.2, [P2])
  *   dcp_lse_merge            -- exact log-sum-exp recombination of the partials ([P1] 5.2, [P2])
  * plus dcp_filter_page_indices (the source-side index filter of [P1] 6.2/6.3 on its own) and
- * dcp_layer_range (the layer split of [P1] 4.1, a host function).
+ * dcp_layer_range (the layer split of [P1] 4.1, a host function).  Around them:
+ *   dcp_decode_attn_merged   -- attention of every rank and the merge in one call
+ *   dcp_attn_plan, dcp_*_run -- the attention's plan made once, then run per layer
+ *   dcp_token_reshard, dcp_partial_decode_attn_tokens -- the token-interleaved layout ([P2])
+ *   dcp_naive_full_transfer, dcp_naive_inplace_shard  -- [P1] 6.1's initial design (baseline)
+ *   dcp_pack_pages, dcp_unpack_pages                  -- bounded pack mode of one path ([P3])
+ *   dcp_partial_decode_attn_static -- the attention without a caller workspace
  *
  * Conventions shared by every entry point:
  *   - KV rows are 576 elements (512 latent + 64 rope, [P1] 5.3); V is the first 512 of them.
@@ -23,15 +29,19 @@
  *     page = 36,864 bytes.  Pool bases must be 16-byte aligned.
  *   - A "page value" v is the decode-side global page number: v = slot * N_dcp + owner.
  *   - Pointers are device pointers unless the comment says host.  The caller owns every
- *     buffer; the library allocates nothing and keeps no state between calls.  Outputs must
- *     not alias inputs.
+ *     buffer; the library allocates nothing and keeps no state between calls, except
+ *     dcp_partial_decode_attn_static's fixed scratch array (see there).  Outputs must not
+ *     alias inputs.
  *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).  Argument and
  *     shape errors are detected on the host before anything is launched and return a
  *     negative dcp_status.  Problems only visible on the device (a page value or index
  *     outside its pool, a pipeline wait that ran past its time limit) are OR-ed into the
  *     optional device word `dev_error` (DCP_DEVERR_* bits; pass NULL to ignore) and the
  *     offending page is skipped; nothing traps.  Read the word after synchronising.
- *   - Thread-safe: no global mutable state.
+ *   - Thread-safe: no global mutable state other than two caches filled once (the driver entry
+ *     point that encodes TMA descriptors, by thread-safe static initialisation; the static
+ *     scratch array's address per device, under a lock).  Calls on one caller-owned workspace
+ *     must not overlap on the GPU.
  */
 #ifndef DCP_H_
 #define DCP_H_
