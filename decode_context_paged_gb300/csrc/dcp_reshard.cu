@@ -67,10 +67,14 @@ __global__ void __launch_bounds__(32, 1) reshard_kernel(const __grid_constant__ 
 // Token-interleaved layout ("SGLang's path": rank d holds tokens d, d + N, d + 2N, ...): every
 // destination local page (layer l, entry e = jj N + d of request b) gathers its 64 rows, row i
 // being token t = (64 jj + i) N + d, from row t mod 64 of the request's source page t div 64 of
-// the CP rank that owns layer l.  One block per destination page (grid-stride), 16-byte vectors.
+// the CP rank that owns layer l.  One block per destination page (grid-stride): the page's 64
+// source row offsets go to shared memory first, then every thread keeps kTokUnroll 16-byte loads
+// in flight before their stores.
 constexpr int kTokThreads = 256;
+constexpr int kTokUnroll = 8;
 
 __global__ void __launch_bounds__(kTokThreads) token_reshard_kernel(const __grid_constant__ TokenReshardArgs a) {
+    __shared__ int64_t row_src[64];  // byte offset of row i's source row in its layer, or -1
     grid_dep_wait();
     grid_dep_launch();
     const int n = a.n_dcp <= 1 ? 1 : a.n_dcp;
@@ -93,29 +97,51 @@ __global__ void __launch_bounds__(kTokThreads) token_reshard_kernel(const __grid
         const int32_t v = __ldg(a.tok_vpages + eg);
         const int64_t slot = a.n_dcp <= 1 ? (int64_t)v : (int64_t)(v / a.n_dcp);
         const int owner = a.n_dcp <= 1 ? 0 : (int)(v % a.n_dcp);
-        if (v < 0 || owner != d || slot >= a.dst_slots) {
+        if (v < 0 || owner != d || slot >= a.dst_slots) {  // uniform over the block
             if (threadIdx.x == 0 && a.dev_error) atomicOr(a.dev_error, DCP_DEVERR_OUT_OF_RANGE);
             continue;
         }
         int r = 0;
         while (r + 1 < a.n_cp && l >= a.layer_start[r + 1]) ++r;
-        const int64_t n_b = __ldg(a.seq_lens + b);
-        const int64_t sp0 = __ldg(a.src_page_ptr + b);
+        if (threadIdx.x < 64) {
+            const int i = threadIdx.x;
+            const int64_t t = (64 * jj + i) * n + d;
+            int64_t off = -1;
+            if (t < (int64_t)__ldg(a.seq_lens + b)) {
+                const int32_t sp = __ldg(a.src_pages + __ldg(a.src_page_ptr + b) + t / 64);
+                if (sp < 0 || sp >= a.src_pool_pages) {
+                    if (a.dev_error) atomicOr(a.dev_error, DCP_DEVERR_OUT_OF_RANGE);
+                } else {
+                    off = (int64_t)sp * page_bytes + (t % 64) * a.row_bytes;
+                }
+            }
+            row_src[i] = off;
+        }
+        __syncthreads();
         uint8_t *dst = a.dst_pools[d] + ((int64_t)l * a.dst_slots + slot) * page_bytes;
         const uint8_t *src_layer = a.src_pools[r] + (int64_t)(l - a.layer_start[r]) * a.src_pool_pages * page_bytes;
-        for (int idx = threadIdx.x; idx < 64 * vecs; idx += blockDim.x) {
-            const int i = idx / vecs, c = idx - i * vecs;
-            const int64_t t = (64 * jj + i) * n + d;
-            if (t >= n_b) continue;
-            const int32_t sp = __ldg(a.src_pages + sp0 + t / 64);
-            if (sp < 0 || sp >= a.src_pool_pages) {
-                if (a.dev_error) atomicOr(a.dev_error, DCP_DEVERR_OUT_OF_RANGE);
-                continue;
+        const int total = 64 * vecs;
+        for (int base = threadIdx.x; base < total; base += kTokUnroll * kTokThreads) {
+            uint4 x[kTokUnroll];
+            int dst_vec[kTokUnroll];  // vector index within the destination page, or -1
+#pragma unroll
+            for (int u = 0; u < kTokUnroll; ++u) {
+                const int idx = base + u * kTokThreads;
+                dst_vec[u] = -1;
+                if (idx < total) {
+                    const int i = idx / vecs, c = idx - i * vecs;
+                    const int64_t off = row_src[i];
+                    if (off >= 0) {
+                        x[u] = __ldg(reinterpret_cast<const uint4 *>(src_layer + off) + c);
+                        dst_vec[u] = idx;
+                    }
+                }
             }
-            const uint4 x = __ldg(reinterpret_cast<const uint4 *>(src_layer + (int64_t)sp * page_bytes +
-                                                                  (t % 64) * a.row_bytes) + c);
-            reinterpret_cast<uint4 *>(dst + (int64_t)i * a.row_bytes)[c] = x;
+#pragma unroll
+            for (int u = 0; u < kTokUnroll; ++u)
+                if (dst_vec[u] >= 0) reinterpret_cast<uint4 *>(dst)[dst_vec[u]] = x[u];
         }
+        __syncthreads();  // row_src is rewritten by the next item
     }
 }
 
