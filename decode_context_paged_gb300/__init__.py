@@ -91,6 +91,8 @@ def _load():
         lib.dcp_decode_attn_merged_run.restype = i32
         lib.dcp_lse_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp, vp]
         lib.dcp_lse_merge.restype = i32
+        lib.dcp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp, vp]
+        lib.dcp_selftest_wait_timeout.restype = i32
         _lib = lib
     return _lib
 
@@ -438,3 +440,11 @@ def lse_merge(o_part: torch.Tensor, lse_part: torch.Tensor, o_out: torch.Tensor 
                                  _stream(stream)),
            "dcp_lse_merge")
     return o_out, lse_out
+
+
+def selftest_wait_timeout(limit_ns: int, dev_error: torch.Tensor, out_ok: torch.Tensor, stream=None) -> None:
+    """Run the library's bounded pipeline wait on a barrier nothing completes (see dcp.h):
+    afterwards dev_error has DEVERR_TIMEOUT set and out_ok holds 0."""
+    _check(_load().dcp_selftest_wait_timeout(int(limit_ns), _dptr(dev_error, "dev_error", torch.int32),
+                                             _dptr(out_ok, "out_ok", torch.int32), _stream(stream)),
+           "dcp_selftest_wait_timeout")

@@ -365,6 +365,18 @@ int dcp_partial_decode_attn_static(int num_requests, int q_len, int num_heads, c
 int dcp_lse_merge(int n_parts, int64_t rows, int v_dim, const float *o_part,
                   const float *lse_part, float *o_out, float *lse_out, dcp_stream_t stream);
 
+/*
+ * Self-test of the device-side failure path (the pages have no counterpart).  Every pipeline
+ * wait in the library gives up after a wall-time limit (DCP_WAIT_LIMIT_NS, default 2 s), sets
+ * DCP_DEVERR_TIMEOUT in the caller's error word and lets the kernel return instead of hanging.
+ * This call runs that same wait, for limit_ns, on a barrier that nothing ever completes: after
+ * it, *dev_error has the DCP_DEVERR_TIMEOUT bit set and *out_ok holds 0 (1 would mean the wait
+ * completed).  dev_error and out_ok are device int32 words; dev_error is OR-ed into, out_ok is
+ * written.  The context stays usable.  Returns DCP_ERR_INVALID_ARG for limit_ns == 0 or above
+ * 1e9 (one second) or a null pointer; DCP_ERR_CUDA if the launch fails.
+ */
+int dcp_selftest_wait_timeout(uint64_t limit_ns, int32_t *dev_error, int32_t *out_ok, dcp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
