@@ -41,8 +41,8 @@ L2_BYTES = 129 << 20  # GB300 L2
 NCU_TRAFFIC = {
     # (kernel, workload): (source hash, DRAM bytes per launch)
     ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("291728be04d95f89", 552155136),
-    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("68f9b5162613d53d", 327527168),
-    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("68f9b5162613d53d", 3068039480),
+    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("0216ffde59f763ae", 327148288),
+    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("0216ffde59f763ae", 3068612312),
 }
 
 
