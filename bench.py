@@ -299,13 +299,18 @@ class Workload:
 
 
 def dist_setup():
+    """One process per GPU under torchrun (NCCL); gloo on a host without CUDA (the oracle arm,
+    and the CPU tests of this logic)."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
         import torch.distributed as dist
         rank = int(os.environ["RANK"])
         local = int(os.environ.get("LOCAL_RANK", rank))
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
         return dist, rank, ws, local
     return None, 0, 1, 0
 
@@ -318,7 +323,8 @@ def barrier(dist):
 def max_over_ranks(dist, x: float) -> float:
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
