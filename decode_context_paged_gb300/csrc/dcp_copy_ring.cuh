@@ -9,9 +9,15 @@
 
 namespace dcp {
 
+#ifndef DCP_RING_STAGES
+#define DCP_RING_STAGES 11
+#endif
+#ifndef DCP_RING_LAG
+#define DCP_RING_LAG 8
+#endif
 constexpr uint32_t kRingChunk = 18432;  // divides both page sizes (73,728 and 36,864 bytes)
-constexpr int kRingStages = 11;
-constexpr int kRingLag = 8;             // loads kept ahead of stores
+constexpr int kRingStages = DCP_RING_STAGES;
+constexpr int kRingLag = DCP_RING_LAG;  // loads kept ahead of stores
 static_assert(kRingStages - kRingLag - 1 >= 0, "ring too small for the lag");
 constexpr size_t kRingSmem = (size_t)kRingStages * kRingChunk + kRingStages * sizeof(uint64_t);
 
