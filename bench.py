@@ -43,6 +43,7 @@ NCU_TRAFFIC = {
     ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("291728be04d95f89", 552155136),
     ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("0216ffde59f763ae", 327148288),
     ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("0216ffde59f763ae", 3068612312),
+    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("0216ffde59f763ae", 2590591776),
 }
 
 
