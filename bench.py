@@ -41,9 +41,9 @@ L2_BYTES = 129 << 20  # GB300 L2
 NCU_TRAFFIC = {
     # (kernel, workload): (source hash, DRAM bytes per launch)
     ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("291728be04d95f89", 552155136),
-    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("0216ffde59f763ae", 327148288),
-    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("0216ffde59f763ae", 3068612312),
-    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("0216ffde59f763ae", 2590591776),
+    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("13cee4b784b09fbf", 327778560),
+    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("13cee4b784b09fbf", 3069808456),
+    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("13cee4b784b09fbf", 2584314280),
 }
 
 

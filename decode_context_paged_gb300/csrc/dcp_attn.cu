@@ -1317,7 +1317,6 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
 
     int32_t *tile_cnt = reinterpret_cast<int32_t *>(ws + s.off_tiles);
     int32_t *multi_list = reinterpret_cast<int32_t *>(ws + s.off_multi);
-    const bool fused = a.o_out != nullptr;
     // blocks per request: about three blocks per SM in all, at most one per tile
     const int tile_stride = (int)std::max<long long>(
         1, std::min<long long>(s.tiles_per_req, (3LL * num_sms + s.B - 1) / s.B));
