@@ -77,3 +77,33 @@ def test_merged_consecutive_calls_reuse_workspace(cuda_device):
     for _ in range(3):
         again = _run(case, ws)[:2]
         assert torch.equal(first[0], again[0]) and torch.equal(first[1], again[1])
+
+
+@pytest.mark.gpu
+def test_control_gather_and_merge_on_a_one_rank_nccl_group(cuda_device, monkeypatch):
+    """The per-layer exchange of the multi-GPU deployment (all-gather of the partials, then the
+    library's merge) through a real NCCL group; one GPU per box here, so one rank holding every
+    DCP partial as its own rows' stack is gathered and merged."""
+    import socket
+
+    import torch.distributed as dist
+
+    from decode_context_paged_gb300 import control
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    monkeypatch.setenv("MASTER_ADDR", "127.0.0.1")
+    monkeypatch.setenv("MASTER_PORT", str(port))
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=cuda_device)
+    try:
+        case = di.attention_case([900, 70], H=16, T=1, n_dcp=1, dtype="bf16", slots_per_rank=None, seed=12,
+                                 device=cuda_device, name="nccl-1")
+        o, lse = dcp.partial_decode_attn(case.q, case.seq_lens, case.req_page_ptr, case.dst_vpages, case.pools,
+                                         case.softmax_scale)
+        R = case.rows
+        om, lm = control.gather_and_merge(o[0].reshape(R, 512), lse[0].reshape(R))
+        torch.cuda.synchronize()
+        ro, rl = oracle_attention(case, qb=q_bits(case), pools=pool_bytes(case))
+        compare(om.cpu().numpy().reshape(R, 512), lm.cpu().numpy().reshape(R), ro, rl, "nccl gather + merge")
+    finally:
+        dist.destroy_process_group()
