@@ -1245,20 +1245,28 @@ bool plan_attention(int B, int T, int H, int N, int64_t num_pages, int dtype, in
     s->G = T * HB;
     s->heads_per_group = std::min(H, kGroupRows);
     s->num_pages = num_pages;
-    // Chunk size: equal-segment cost model, makespan in tiles with a partial round trip
-    // (write + read of a 64 x 512 fp32 chunk output, in tile-equivalents of KV bytes).
+    // Chunk size: equal-segment cost model, makespan in tiles over num_sms persistent CTAs taking
+    // units from a queue.  A chunk boundary costs the round trip of a partial (write + read of a
+    // 64 x 512 fp32 chunk output, in tile-equivalents of KV bytes) plus about one tile of
+    // epilogue and restart.  A last wave that keeps a fraction f of the SMs busy takes (1 + f) / 2
+    // of a full wave: the kernel is bound by memory latency, which drops with the load (measured
+    // on the 48 x 100K FP8 workload: unchunked units beat the 3-chunk split a whole-wave count
+    // picks by 4%, while the 4 x 1M workload keeps its 7-chunk split).
     const long long pages_avg = B > 0 ? (num_pages + B - 1) / B : 0;
     const long long tiles_seg = std::max<long long>(1, ((pages_avg + N - 1) / N + 1) / 2);
     const long long n_seg = (long long)N * B * s->G;
     const double partial_cost = (2.0 * kGroupRows * kVDim * 4.0) / (128.0 * kKDim * (dtype == DCP_KV_BF16 ? 2 : 1));
+    const double chunk_cost = partial_cost + 1.0;
     double best = 1e300;
     long long tpc = tiles_seg;
     for (long long k = 1; k <= std::min<long long>(tiles_seg, 64); ++k) {
         const long long t = (tiles_seg + k - 1) / k;
         const long long chunks = (tiles_seg + t - 1) / t;
         const long long units = std::max<long long>(1, n_seg * chunks);
-        const long long waves = (units + num_sms - 1) / num_sms;
-        const double cost = (double)waves * ((double)t + (chunks > 1 ? partial_cost : 0.0));
+        const long long full = units / num_sms;
+        const double f = (double)(units - full * num_sms) / num_sms;
+        const double waves = (double)full + (f > 0.0 ? 0.5 + 0.5 * f : 0.0);
+        const double cost = waves * ((double)t + (chunks > 1 ? chunk_cost : 0.0));
         if (cost < best - 1e-9) {
             best = cost;
             tpc = t;
