@@ -1272,6 +1272,15 @@ bool plan_attention(int B, int T, int H, int N, int64_t num_pages, int dtype, in
             tpc = t;
         }
     }
+    // With at least as many segments as SMs, segments of unequal length (the host sees only
+    // their average) balance by themselves in the largest-first queue, so a chunk may grow to a
+    // fair part of each SM's share of all tiles (measured on 64 requests of 2K to 500K tokens:
+    // chunks from 0.55 to 1.0 of the share run within 2% of each other, 1.25 of it 12% slower,
+    // the average-segment size 4% slower).
+    if (n_seg >= num_sms) {
+        const long long share = (long long)std::ceil(0.6 * (double)(n_seg * tiles_seg) / num_sms);
+        tpc = std::max(tpc, share);
+    }
     tpc = std::max<long long>(1, std::min<long long>(tpc, kMaxTpc));
     s->tiles_per_chunk = (int)tpc;
     s->max_partials = ((long long)s->G * (num_pages + (long long)N * B)) / tpc + s->G;
