@@ -41,9 +41,9 @@ L2_BYTES = 129 << 20  # GB300 L2
 NCU_TRAFFIC = {
     # (kernel, workload): (source hash, DRAM bytes per launch)
     ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("8d0f9cf32f21b0c0", 550526592),
-    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("13cee4b784b09fbf", 327778560),
-    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("13cee4b784b09fbf", 3069808456),
-    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("13cee4b784b09fbf", 2584314280),
+    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("cdc1671979cd698a", 328198912),
+    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("cdc1671979cd698a", 2916891744),
+    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("cdc1671979cd698a", 2587413368),
 }
 
 
