@@ -37,20 +37,24 @@ L2_BYTES = 129 << 20  # GB300 L2
 
 # DRAM bytes per launch measured by ncu (dram__bytes_read.sum + dram__bytes_write.sum) for the
 # kernels below on the default workload, with the hash of the kernel source they were taken
-# on; a changed source reports traffic null until it is re-measured.
+# on (for the reshard: dcp_reshard.cu and the copy ring header); a changed source reports
+# traffic null until it is re-measured.
 NCU_TRAFFIC = {
     # (kernel, workload): (source hash, DRAM bytes per launch)
-    ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("8d0f9cf32f21b0c0", 550526592),
+    ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("669d0ca9bde09661", 551785600),
     ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("cdc1671979cd698a", 328198912),
     ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("cdc1671979cd698a", 2916891744),
     ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("cdc1671979cd698a", 2587413368),
 }
 
 
-def _src_hash(name: str) -> str:
-    p = os.path.join(ROOT, "decode_context_paged_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def _src_hash(names) -> str:
+    """sha256/16 of one kernel source file, or of several concatenated in order."""
+    h = hashlib.sha256()
+    for name in ([names] if isinstance(names, str) else names):
+        with open(os.path.join(ROOT, "decode_context_paged_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def peaks():
@@ -542,7 +546,7 @@ def run_ours(args):
     attn_tflops = wl.flops_attn / (stage_ms["attn"] * 1e-3) / 1e12
     dom = max(stage_ms, key=stage_ms.get)
     kernel_of = {"reshard": "reshard_kernel", "attn": "attn_kernel", "merge": "lse_merge_kernel"}
-    src_of = {"reshard": "dcp_reshard.cu", "attn": "dcp_attn.cu", "merge": "dcp_merge.cu"}
+    src_of = {"reshard": ("dcp_reshard.cu", "dcp_copy_ring.cuh"), "attn": "dcp_attn.cu", "merge": "dcp_merge.cu"}
     tr = NCU_TRAFFIC.get((kernel_of[dom], wl.name))
     traffic = tr[1] if tr and tr[0] == _src_hash(src_of[dom]) else None
     # the tensor roofline uses the peak of the MMA kind executed (kind::f8f6f4 = 2x the BF16 rate)

@@ -10,12 +10,18 @@
 namespace dcp {
 
 #ifndef DCP_RING_STAGES
-#define DCP_RING_STAGES 11
+#define DCP_RING_STAGES 6
 #endif
 #ifndef DCP_RING_LAG
-#define DCP_RING_LAG 8
+#define DCP_RING_LAG 3
 #endif
-constexpr uint32_t kRingChunk = 18432;  // divides both page sizes (73,728 and 36,864 bytes)
+#ifndef DCP_RING_CHUNK
+#define DCP_RING_CHUNK 36864
+#endif
+// The largest chunk that divides both page sizes (73,728 and 36,864 bytes): fewer, larger bulk
+// copies move more bytes per issue (measured: 36 KB x 6 stages beats 18 KB x 11 by 4-7%, 9 KB
+// x 23 is 30% slower).
+constexpr uint32_t kRingChunk = DCP_RING_CHUNK;
 constexpr int kRingStages = DCP_RING_STAGES;
 constexpr int kRingLag = DCP_RING_LAG;  // loads kept ahead of stores
 static_assert(kRingStages - kRingLag - 1 >= 0, "ring too small for the lag");
