@@ -11,6 +11,17 @@ Entry points (same names as the C ABI):
   reshard_pages            CP layer-split -> DCP page reshard, all paths in one launch (2, 6.3, 6.4)
   partial_decode_attn      per-rank paged MLA decode attention -> partial O + LSE (5.2)
   lse_merge                exact LSE merge of the partials (5.2)
+  decode_attn_merged       every rank's attention and the merge in one call
+  attn_plan                the attention's plan, made once and run per layer (planned=True)
+  token_reshard            reshard into the token-interleaved layout ("SGLang's path"); the
+                           attention over it: partial_decode_attn(layout="token")
+  naive_full_transfer,     the initial design kept as a baseline (6.1): full KV to every DCP rank,
+  naive_inplace_shard        then an in-place shard
+  pack_pages, unpack_pages one path's pages through a bounded staging buffer (pack_chunks plans it)
+  partial_decode_attn_static  the attention without a caller workspace
+  selftest_wait_timeout    runs the bounded device wait to its limit (failure-path test)
+The host-side multi-rank control (bootstrap, size broadcast, consensus prefix, exchange) is in
+``decode_context_paged_gb300.control``.
 """
 from __future__ import annotations
 
