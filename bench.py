@@ -7,6 +7,13 @@ on every DCP rank, and the exact LSE merge.  Default workload: 32 requests x 819
 The attention and the merge run as one library call (dcp_decode_attn_merged); --unfused
 times dcp_partial_decode_attn and dcp_lse_merge as separate calls.
 
+Timing: after the warm-up and a half-second soak of the same step (under which nvidia-smi
+samples the clocks), K steps between two CUDA events give the value; a second pass of K steps
+with events around every stage gives the stage times and the roofline's kernel duration.  The
+end-to-end number runs the step through the same calls with the inputs uploaded from pinned
+host memory every step (double-buffered, the next step's upload on a copy stream) and the
+merged output read back.
+
 Prints one JSON line.  --impl reference times the float64 CPU oracle instead (bounded
 sample of the same workload, on the host cores).
 """
@@ -614,9 +621,12 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=sorted(WORKLOADS), default="batch")
-    ap.add_argument("--ref-seconds", type=float, default=15.0)
-    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--config", choices=sorted(WORKLOADS), default="batch",
+                    help="batch: 32 x 8192 BF16; agent: 48 x 100K E4M3; long: 4 x 1M, q_len 4, E4M3; e2e: 64 "
+                         "requests of 2K-500K, 8 layers, CP4 -> DCP8, E4M3; tiny: 1 x 1024 (a check, not a bench)")
+    ap.add_argument("--ref-seconds", type=float, default=15.0,
+                    help="host-time budget of one oracle sample (cpu_baseline; per step of --impl reference at most)")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle sample in the CUDA arm")
     ap.add_argument("--layout", choices=["page", "token"], default="page",
                     help="token: token-interleaved DCP (rank i holds tokens i, i + N, ...) instead of pages")
     ap.add_argument("--naive", action="store_true",
