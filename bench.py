@@ -149,11 +149,10 @@ class Workload:
                  naive: bool = False, layout: str = "page", overlap_plan: bool = True):
         import decode_context_paged_gb300 as dcp
         self.layout = layout  # "token": token-interleaved DCP (row-gather reshard, token-layout attention)
-        fused = fused and layout == "page"
         self.fused = fused
         # the attention's plan depends only on the page table: made once per step on a side stream
         # while the reshard runs, then run for every layer
-        self.overlap_plan = overlap_plan and fused and device.type == "cuda"
+        self.overlap_plan = overlap_plan and fused and layout == "page" and device.type == "cuda"
         self.side = torch.cuda.Stream(device) if self.overlap_plan else None
         self.naive = naive  # reshard stage as the pages' initial design: full transfer, then in-place shard
         self.pack = staging_mb > 0  # reshard stage in bounded pack mode (per path: filter, pack, unpack)
@@ -294,11 +293,12 @@ class Workload:
             torch.cuda.current_stream().wait_stream(self.side)
         for l in range(self.L):
             if self.fused:
-                rec("attn", lambda: dcp.decode_attn_merged(q, self.seq_lens, rc.req_page_ptr, rc.dst_vpages,
+                tbl = (self.tok_ptr, self.tok_vp) if self.layout == "token" else (rc.req_page_ptr, rc.dst_vpages)
+                rec("attn", lambda: dcp.decode_attn_merged(q, self.seq_lens, tbl[0], tbl[1],
                                                            self.layer_pools[l], self.scale, self.kv_scale,
                                                            o_part=self.o_part, lse_part=self.lse_part, o_out=self.o[l],
                                                            lse_out=self.lse[l], workspace=self.ws, dev_error=self.err,
-                                                           planned=self.overlap_plan))
+                                                           planned=self.overlap_plan, layout=self.layout))
                 continue
             tbl = (self.tok_ptr, self.tok_vp) if self.layout == "token" else (rc.req_page_ptr, rc.dst_vpages)
             rec("attn", lambda: dcp.partial_decode_attn(q, self.seq_lens, tbl[0], tbl[1],

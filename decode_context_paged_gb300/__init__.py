@@ -100,6 +100,8 @@ def _load():
         lib.dcp_decode_attn_merged.restype = i32
         lib.dcp_decode_attn_merged_run.argtypes = lib.dcp_decode_attn_merged.argtypes
         lib.dcp_decode_attn_merged_run.restype = i32
+        lib.dcp_decode_attn_merged_tokens.argtypes = lib.dcp_decode_attn_merged.argtypes
+        lib.dcp_decode_attn_merged_tokens.restype = i32
         lib.dcp_lse_merge.argtypes = [i32, i64, i32, vp, vp, vp, vp, vp]
         lib.dcp_lse_merge.restype = i32
         lib.dcp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp, vp]
@@ -356,10 +358,15 @@ def decode_attn_merged(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: to
                        o_part: torch.Tensor | None = None, lse_part: torch.Tensor | None = None,
                        o_out: torch.Tensor | None = None, lse_out: torch.Tensor | None = None,
                        workspace: torch.Tensor | None = None, dev_error: torch.Tensor | None = None, stream=None,
-                       planned: bool = False):
+                       planned: bool = False, layout: str = "page"):
     """Every rank's partial attention plus their exact LSE merge in one call (planned: run the
-    plan attn_plan stored in ``workspace``, dcp_decode_attn_merged_run).
+    plan attn_plan stored in ``workspace``, dcp_decode_attn_merged_run; layout "token": the page
+    table is token-interleaved, dcp_decode_attn_merged_tokens).
     Returns (o_out [B][T][H][512], lse_out [B][T][H], o_part, lse_part), all fp32."""
+    if layout not in ("page", "token"):
+        raise ValueError("layout must be 'page' or 'token'")
+    if planned and (workspace is None or layout == "token"):
+        raise ValueError("a planned run needs the workspace holding the plan (page layout)")
     B, T, H, kd = q.shape
     if kd != K_DIM:
         raise ValueError("q must be [B][T][H][576]")
@@ -382,9 +389,8 @@ def decode_attn_merged(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: to
     if workspace is None:
         workspace = alloc_workspace(B, T, H, N, num_pages, dev)
     kp = _ptr_array(kv_pools, "kv_pools")
-    if planned and workspace is None:
-        raise ValueError("a planned run needs the workspace holding the plan")
-    fn = _load().dcp_decode_attn_merged_run if planned else _load().dcp_decode_attn_merged
+    fn = (_load().dcp_decode_attn_merged_run if planned else
+          _load().dcp_decode_attn_merged_tokens if layout == "token" else _load().dcp_decode_attn_merged)
     _check(fn(B, T, H, _dptr(q, "q", torch.bfloat16),
                                           _dptr(seq_lens, "seq_lens", torch.int32),
                                           _dptr(req_page_ptr, "req_page_ptr", torch.int64), num_pages,

@@ -417,6 +417,19 @@ int dcp_decode_attn_merged_run(int num_requests, int q_len, int num_heads, const
                              lse_part, o_out, lse_out, workspace, workspace_bytes, dev_error, stream, 0, 2);
 }
 
+int dcp_decode_attn_merged_tokens(int num_requests, int q_len, int num_heads, const void *q,
+                                  const int32_t *seq_lens, const int64_t *req_page_ptr, int64_t num_pages,
+                                  const int32_t *dst_vpages, int page_size, int dtype, float kv_scale,
+                                  float softmax_scale, int n_dcp, const void *const *kv_pools,
+                                  int64_t slots_per_rank, float *o_part, float *lse_part, float *o_out,
+                                  float *lse_out, void *workspace, size_t workspace_bytes,
+                                  int32_t *dev_error, dcp_stream_t stream) {
+    if (num_requests > 0 && (!o_out || !lse_out || !aligned(o_out, 16))) return DCP_ERR_INVALID_ARG;
+    return partial_attn_impl(num_requests, q_len, num_heads, q, seq_lens, req_page_ptr, num_pages, dst_vpages,
+                             page_size, dtype, kv_scale, softmax_scale, n_dcp, kv_pools, slots_per_rank, -1, o_part,
+                             lse_part, o_out, lse_out, workspace, workspace_bytes, dev_error, stream, 1);
+}
+
 int dcp_decode_attn_merged(int num_requests, int q_len, int num_heads, const void *q,
                            const int32_t *seq_lens, const int64_t *req_page_ptr, int64_t num_pages,
                            const int32_t *dst_vpages, int page_size, int dtype, float kv_scale,

@@ -164,6 +164,16 @@ int dcp_token_reshard(int num_requests, const int32_t *seq_lens, const int64_t *
                       const void *const *src_pools, int64_t src_pool_pages, int n_dcp,
                       void *const *dst_pools, int64_t dst_slots_per_rank, int32_t *dev_error,
                       dcp_stream_t stream);
+/* dcp_decode_attn_merged over a token-interleaved table: every rank's partial as
+ * dcp_partial_decode_attn_tokens, then the merge exactly as dcp_decode_attn_merged (same arguments
+ * and statuses as dcp_decode_attn_merged). */
+int dcp_decode_attn_merged_tokens(int num_requests, int q_len, int num_heads, const void *q,
+                                  const int32_t *seq_lens, const int64_t *req_page_ptr, int64_t num_pages,
+                                  const int32_t *dst_vpages, int page_size, int dtype, float kv_scale,
+                                  float softmax_scale, int n_dcp, const void *const *kv_pools,
+                                  int64_t slots_per_rank, float *o_part, float *lse_part, float *o_out,
+                                  float *lse_out, void *workspace, size_t workspace_bytes,
+                                  int32_t *dev_error, dcp_stream_t stream);
 int dcp_partial_decode_attn_tokens(int num_requests, int q_len, int num_heads, const void *q,
                                    const int32_t *seq_lens, const int64_t *req_page_ptr,
                                    int64_t num_pages, const int32_t *dst_vpages, int page_size,

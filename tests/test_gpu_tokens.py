@@ -81,3 +81,22 @@ def test_token_reshard_matches_oracle_bit_exact(cuda_device, dtype):
                                 rc.src_pool_pages, N, ref, slots) == 0
     for a, b in zip(dst, ref):
         assert np.array_equal(a.cpu().view(torch.uint8).numpy().reshape(-1), b)
+
+
+@pytest.mark.parametrize("name,lens,H,T,N,dtype", [CASES[0], CASES[1], CASES[4]], ids=["ragged", "causal-q4", "ragged-fp8"])
+def test_token_layout_fused_call_matches_oracle(cuda_device, name, lens, H, T, N, dtype):
+    """dcp_decode_attn_merged_tokens: every rank's partial over the token-interleaved table and
+    the merge in one call."""
+    case = di.token_attention_case(lens, H=H, T=T, n_dcp=N, dtype=dtype, seed=11 + len(name), device=cuda_device,
+                                   name=name)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    om, lm, o, l = dcp.decode_attn_merged(case.q, case.seq_lens, case.req_page_ptr, case.dst_vpages, case.pools,
+                                          case.softmax_scale, case.kv_scale, dev_error=err, layout="token")
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    R = case.rows
+    for d in range(N):
+        ro, rl = _oracle(case, rank=d)
+        compare(o[d].cpu().numpy().reshape(R, 512), l[d].cpu().numpy().reshape(R), ro, rl, f"{name} fused rank {d}")
+    ro, rl = _oracle(case)
+    compare(om.cpu().numpy().reshape(R, 512), lm.cpu().numpy().reshape(R), ro, rl, f"{name} fused merged")
