@@ -18,7 +18,8 @@
  * dcp_layer_range (the layer split of [P1] 4.1, a host function).  Around them:
  *   dcp_decode_attn_merged   -- attention of every rank and the merge in one call
  *   dcp_attn_plan, dcp_*_run -- the attention's plan made once, then run per layer
- *   dcp_token_reshard, dcp_partial_decode_attn_tokens -- the token-interleaved layout ([P2])
+ *   dcp_token_reshard, dcp_partial_decode_attn_tokens, dcp_decode_attn_merged_tokens
+ *                            -- the token-interleaved layout ([P2])
  *   dcp_naive_full_transfer, dcp_naive_inplace_shard  -- [P1] 6.1's initial design (baseline)
  *   dcp_pack_pages, dcp_unpack_pages                  -- bounded pack mode of one path ([P3])
  *   dcp_partial_decode_attn_static -- the attention without a caller workspace
