@@ -14,7 +14,7 @@ Entry points (same names as the C ABI):
   decode_attn_merged       every rank's attention and the merge in one call
   attn_plan                the attention's plan, made once and run per layer (planned=True)
   token_reshard            reshard into the token-interleaved layout ("SGLang's path"); the
-                           attention over it: partial_decode_attn(layout="token")
+                           attention over it: partial_decode_attn / decode_attn_merged(layout="token")
   naive_full_transfer,     the initial design kept as a baseline (6.1): full KV to every DCP rank,
   naive_inplace_shard        then an in-place shard
   pack_pages, unpack_pages one path's pages through a bounded staging buffer (pack_chunks plans it)
