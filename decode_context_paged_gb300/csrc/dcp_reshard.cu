@@ -300,12 +300,25 @@ filter_kernel(int64_t n, const int32_t *__restrict__ dst_vpages,
 
 }  // namespace
 
+// CTAs of the copy-ring kernels for a copy of `bytes` (read + write).  Long copies run one CTA per
+// pair of SMs: measured on GB300 (152 SMs), 76 streaming CTAs beat 152 by 4-6% on copies of 5 to
+// 53 GB (the reshard reaches 99-100% of the copy peak) and 60 to 114 CTAs land in between
+// (plausibly the two SMs of a pair share their way to memory, so a second stream on a pair adds
+// queueing rather than bandwidth).  Short copies keep one CTA per SM: on a 0.6 GB reshard inside
+// a decode step, 152 CTAs are 1-2% faster (the shorter ramp counts more).  The switch sits at
+// 16 MB per CTA of the half grid.
+inline int ring_ctas(int num_sms, int64_t bytes) {
+    const int half = num_sms > 1 ? num_sms / 2 : 1;
+    return bytes >= (int64_t)half * (16ll << 20) ? half : num_sms;
+}
+
 cudaError_t launch_reshard(const ReshardArgs &a, int num_sms, cudaStream_t stream) {
     if ((a.layer_end - a.layer_begin) <= 0 || a.num_pages <= 0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(reshard_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kRingSmem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(reshard_kernel, dim3(num_sms), dim3(32), kRingSmem, stream, a);
+    const int64_t bytes = 2 * a.num_pages * (int64_t)(a.layer_end - a.layer_begin) * a.page_bytes;
+    return launch_pdl(reshard_kernel, dim3(ring_ctas(num_sms, bytes)), dim3(32), kRingSmem, stream, a);
 }
 
 cudaError_t launch_token_reshard(const TokenReshardArgs &a, int num_sms, cudaStream_t stream) {
@@ -319,7 +332,9 @@ cudaError_t launch_naive(const NaiveArgs &a, int num_sms, cudaStream_t stream) {
     if (a.base.layer_end <= 0 || a.base.num_pages <= 0) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(naive_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(naive_kernel, dim3(num_sms), dim3(32), kRingSmem, stream, a);
+    const int n_dst = a.mode == 0 ? (a.base.n_dcp <= 1 ? 1 : a.base.n_dcp) : 1;
+    const int64_t bytes = 2 * (int64_t)n_dst * a.base.layer_end * a.base.num_pages * a.base.page_bytes;
+    return launch_pdl(naive_kernel, dim3(ring_ctas(num_sms, bytes)), dim3(32), kRingSmem, stream, a);
 }
 
 cudaError_t launch_pack(const PackArgs &a, int num_sms, cudaStream_t stream) {
@@ -327,7 +342,8 @@ cudaError_t launch_pack(const PackArgs &a, int num_sms, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(pack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRingSmem);
     if (e != cudaSuccess) return e;
     const int64_t chunks = a.n_items * (a.page_bytes / kRingChunk);
-    const int grid = (int)(chunks < num_sms ? chunks : num_sms);
+    const int ctas = ring_ctas(num_sms, 2 * a.n_items * a.page_bytes);
+    const int grid = (int)(chunks < ctas ? chunks : ctas);
     return launch_pdl(pack_kernel, dim3(grid), dim3(32), kRingSmem, stream, a);
 }
 
