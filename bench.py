@@ -48,8 +48,8 @@ L2_BYTES = 129 << 20  # GB300 L2
 # traffic null until it is re-measured.
 NCU_TRAFFIC = {
     # (kernel, workload): (source hash, DRAM bytes per launch)
-    ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("d1d033077f70311a", 551931904),
-    ("reshard_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("d1d033077f70311a", 5485639424),
+    ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("688cc21d0eb99b1d", 551600768),
+    ("reshard_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("688cc21d0eb99b1d", 5485940480),
     ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("cdc1671979cd698a", 328198912),
     ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("cdc1671979cd698a", 2916891744),
     ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("cdc1671979cd698a", 2587413368),
