@@ -2,10 +2,13 @@
 
 One step = one pass of the whole path over one batch: the page-level reshard from the CP
 layer-split source layout into the DCP page-interleaved pools, partial MLA decode attention
-on every DCP rank, and the exact LSE merge.  Default workload: 32 requests x 8192 tokens,
-64 heads, q_len 1, BF16 KV, page 64, DCP=8, resharded from one CP source shard (1 layer).
-The attention and the merge run as one library call (dcp_decode_attn_merged); --unfused
-times dcp_partial_decode_attn and dcp_lse_merge as separate calls.
+on every DCP rank, and the exact LSE merge.  Default workload (the largest): 64 requests of
+2K-500K tokens (log-uniform, multiples of 64), 8 layers, FP8-E4M3 KV, page 64, resharded from a
+CP4 layer split into DCP=8, then per layer the attention of 64 heads (q_len 1) on every rank and
+the merge.  The attention's plan is made once per step (it depends only on the page table) on a
+side stream while the reshard runs; the attention and the merge run as one library call per
+layer (dcp_decode_attn_merged_run); --unfused times dcp_partial_decode_attn and dcp_lse_merge
+as separate calls.
 
 Timing: after the warm-up and a half-second soak of the same step (under which nvidia-smi
 samples the clocks), K steps between two CUDA events give the value; a second pass of K steps
@@ -147,13 +150,21 @@ class Workload:
     on every DCP rank and the LSE merge."""
 
     def __init__(self, name: str, device, seed: int = 1, fused: bool = True, staging_mb: int = 0,
-                 naive: bool = False, layout: str = "page", overlap_plan: bool = True):
-        import decode_context_paged_gb300 as dcp
+                 naive: bool = False, layout: str = "page", overlap_plan: bool = True, oracle_only: bool = False):
+        """oracle_only: inputs for the oracle arm -- the layer split from the oracle, no library
+        call, no workspace (that arm loads nothing but the oracle)."""
+        if oracle_only:
+            import oracle
+            split = oracle.layer_range
+            dcp = None
+        else:
+            import decode_context_paged_gb300 as dcp
+            split = dcp.layer_range
         self.layout = layout  # "token": token-interleaved DCP (row-gather reshard, token-layout attention)
         self.fused = fused
         # the attention's plan depends only on the page table: made once per step on a side stream
         # while the reshard runs, then run for every layer
-        self.overlap_plan = overlap_plan and fused and layout == "page" and device.type == "cuda"
+        self.overlap_plan = overlap_plan and fused and layout == "page" and device.type == "cuda" and not oracle_only
         self.side = torch.cuda.Stream(device) if self.overlap_plan else None
         self.naive = naive  # reshard stage as the pages' initial design: full transfer, then in-place shard
         self.pack = staging_mb > 0  # reshard stage in bounded pack mode (per path: filter, pack, unpack)
@@ -161,7 +172,7 @@ class Workload:
         lens = lens_fn()
         self.lens = lens
         self.B = len(lens)
-        counts = [e - s for s, e in (dcp.layer_range(self.L, self.n_cp, r) for r in range(self.n_cp))]
+        counts = [e - s for s, e in (split(self.L, self.n_cp, r) for r in range(self.n_cp))]
         self.rc = di.reshard_case(lens, n_layers=self.L, layer_counts=counts, n_dcp=self.N, dtype=self.dtype,
                                   contiguous_src=True, seed=seed, device=device, dst_slots=slots)
         self.q = di.random_q(self.B, self.T, self.H, di._gen(seed + 7, device), device)
@@ -188,8 +199,9 @@ class Workload:
         self.o = torch.empty((self.L, self.B, self.T, self.H, 512), dtype=torch.float32, device=device)
         self.lse = torch.empty((self.L, self.B, self.T, self.H), dtype=torch.float32, device=device)
         n_entries = self.tok_vp.numel() if layout == "token" else self.rc.dst_vpages.numel()
-        # (the workspace is sized for the device's SM count; the oracle arm on a host has none)
-        self.ws = dcp.alloc_workspace(self.B, self.T, self.H, self.N, n_entries, device) if device.type == "cuda" else None
+        # (the workspace is sized for the device's SM count; the oracle arm has none)
+        self.ws = (dcp.alloc_workspace(self.B, self.T, self.H, self.N, n_entries, device)
+                   if device.type == "cuda" and not oracle_only else None)
         self.err = torch.zeros(1, dtype=torch.int32, device=device)
         pages = self.rc.dst_vpages.numel()
         elem = 2 if self.dtype == "bf16" else 1
@@ -402,7 +414,7 @@ def run_reference(args):
     if rank != 0:
         return
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
-    wl = Workload(args.config, dev)
+    wl = Workload(args.config, dev, oracle_only=True)
     vals, secs, desc, threads = [], [], "", 1
     # the oracle has no warm state: warm-up steps are not run; the whole run stays near two
     # minutes of host time however many steps are asked for
@@ -416,11 +428,40 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": wl.name, "l2": wl.l2_note},
+        "data": "synthetic", "config": workload_config(wl, world),
         "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def workload_config(wl, world: int) -> dict:
+    """The `config` object of both arms' JSON lines."""
+    return {"workload": wl.name, "l2": wl.l2_note, "bytes_per_step": sum(wl.bytes.values()),
+            "parallelism": f"replicas x{world}"}
+
+
+def fp8_dense_peak_tflops(dev, n: int = 8192, reps: int = 10):
+    """Dense E4M3 x E4M3 -> BF16 GEMM throughput of this GPU (cuBLASLt through torch._scaled_mm,
+    n^3, best of `reps`, CUDA events): the tensor roofline of the FP8 contraction.  None if the
+    call is unavailable."""
+    try:
+        a = torch.randn((n, n), device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn((n, n), device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=dev, dtype=torch.float32)
+        for _ in range(3):
+            torch._scaled_mm(a, b, one, one, out_dtype=torch.bfloat16)
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b, one, one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        return 2.0 * n ** 3 / (best * 1e-3) / 1e12
+    except Exception:  # noqa: BLE001 -- the bench falls back to the nominal ratio
+        return None
 
 
 def _stage_ms(events, steps):
@@ -557,13 +598,18 @@ def run_ours(args):
     src_of = {"reshard": ("dcp_reshard.cu", "dcp_copy_ring.cuh"), "attn": "dcp_attn.cu", "merge": "dcp_merge.cu"}
     tr = NCU_TRAFFIC.get((kernel_of[dom], wl.name))
     traffic = tr[1] if tr and tr[0] == _src_hash(src_of[dom]) else None
-    # the tensor roofline uses the peak of the MMA kind executed (kind::f8f6f4 = 2x the BF16 rate)
-    tc_peak = bf16 * (2.0 if wl.dtype == "e4m3" else 1.0)
+    # the tensor roofline uses the peak of the MMA kind executed: E4M3 measured on this GPU (a
+    # cuBLASLt FP8 GEMM), else twice the BF16 peak (the nominal ratio)
+    if wl.dtype == "e4m3":
+        fp8 = fp8_dense_peak_tflops(dev)
+        tc_peak, tc_kind = (fp8, "measured here: cuBLASLt e4m3 8192^3 GEMM, best of 10") if fp8 else (
+            2.0 * bf16, peak_kind + " bf16 x2 (nominal e4m3 ratio)")
+    else:
+        tc_peak, tc_kind = bf16, peak_kind + " bf16"
     attn_bound = "tensor" if wl.flops_attn / tc_peak / 1e12 > wl.stage_bytes["attn"] / hbm / 1e9 else "hbm"
     if dom == "attn" and attn_bound == "tensor":
         roof = {"kernel": "attn_kernel", "bound": "tensor", "achieved": attn_tflops, "peak": tc_peak,
-                "unit": "TFLOP/s", "frac": attn_tflops / tc_peak, "peak_kind": peak_kind + (
-                    " bf16 x2 for kind::f8f6f4" if wl.dtype == "e4m3" else " bf16"),
+                "unit": "TFLOP/s", "frac": attn_tflops / tc_peak, "peak_kind": tc_kind,
                 "traffic": traffic, "algorithmic_flops": wl.flops_attn}
     else:
         roof = {"kernel": kernel_of[dom], "bound": "hbm", "achieved": stage_gbs[dom], "peak": hbm, "unit": "GB/s",
@@ -578,8 +624,7 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "e4m3 (fp32 accumulate)",
         "data": "synthetic",
-        "config": {"workload": wl.name, "l2": wl.l2_note, "bytes_per_step": step_bytes,
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(wl, world),
         "stages": {
             "reshard": {"ms": stage_ms["reshard"], "GB/s": stage_gbs["reshard"], "frac_hbm": stage_gbs["reshard"] / hbm,
                         **({"mode": f"bounded pack, {args.staging_mb} MB staging buffer",
@@ -592,7 +637,8 @@ def run_ours(args):
                            if wl.naive else {"mode": "token-interleaved row gather"} if wl.layout == "token"
                            else {"mode": "direct"})},
             "attn": {"ms": stage_ms["attn"], "GB/s": stage_gbs["attn"], "TFLOP/s": attn_tflops,
-                     "frac_hbm": stage_gbs["attn"] / hbm, "frac_tensor": attn_tflops / tc_peak, "bound": attn_bound,
+                     "frac_hbm": stage_gbs["attn"] / hbm, "frac_tensor": attn_tflops / tc_peak,
+                     "tensor_peak_TFLOP/s": tc_peak, "tensor_peak_kind": tc_kind, "bound": attn_bound,
                      "includes_merge": wl.fused},
             **({} if wl.fused else {"merge": {"ms": stage_ms["merge"], "GB/s": stage_gbs["merge"],
                                               "frac_hbm": stage_gbs["merge"] / hbm}}),
@@ -622,9 +668,10 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", choices=sorted(WORKLOADS), default="batch",
-                    help="batch: 32 x 8192 BF16; agent: 48 x 100K E4M3; long: 4 x 1M, q_len 4, E4M3; e2e: 64 "
-                         "requests of 2K-500K, 8 layers, CP4 -> DCP8, E4M3; tiny: 1 x 1024 (a check, not a bench)")
+    ap.add_argument("--config", choices=sorted(WORKLOADS), default="e2e",
+                    help="e2e (default, the largest workload): 64 requests of 2K-500K, 8 layers, CP4 -> DCP8, "
+                         "E4M3; batch: 32 x 8192 BF16; agent: 48 x 100K E4M3; long: 4 x 1M, q_len 4, E4M3; "
+                         "tiny: 1 x 1024 (a check, not a bench)")
     ap.add_argument("--ref-seconds", type=float, default=15.0,
                     help="host-time budget of one oracle sample (cpu_baseline; per step of --impl reference at most)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle sample in the CUDA arm")

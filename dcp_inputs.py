@@ -67,8 +67,10 @@ def random_q(b: int, t: int, h: int, gen: torch.Generator, device) -> torch.Tens
     return q
 
 
-def page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Generator):
-    """Round-robin ownership with seeded random slots.  Returns (req_page_ptr, dst_vpages)."""
+def page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Generator, with_slots: bool = False):
+    """Round-robin ownership with seeded random slots.  Returns (req_page_ptr, dst_vpages), and
+    with ``with_slots`` also the owner rank and pool slot the generator chose for every entry
+    (int64 CPU tensors), so that tests can address a page's rows without decoding its value."""
     pages = [(int(n) + PAGE - 1) // PAGE for n in seq_lens]
     ptr = [0]
     for p in pages:
@@ -77,6 +79,8 @@ def page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Generator):
     perms = [torch.randperm(slots_per_rank, generator=gen, device="cpu") for _ in range(n_ranks)]
     used = [0] * n_ranks
     vp = torch.empty(ptr[-1], dtype=torch.int64)
+    owners = torch.empty(ptr[-1], dtype=torch.int64)
+    slots_of = torch.empty(ptr[-1], dtype=torch.int64)
     k = 0
     for p in pages:
         j = torch.arange(p)
@@ -89,19 +93,23 @@ def page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Generator):
             slots = perms[d][used[d]:used[d] + cnt]
             used[d] += cnt
             vp[k:k + p][sel] = slots * n_ranks + d if n_dcp > 1 else slots
+            owners[k:k + p][sel] = d
+            slots_of[k:k + p][sel] = slots
         k += p
-    return torch.tensor(ptr, dtype=torch.int64), vp.to(torch.int32)
+    out = (torch.tensor(ptr, dtype=torch.int64), vp.to(torch.int32))
+    return out + (owners, slots_of) if with_slots else out
 
 
-def token_page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Generator):
+def token_page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Generator, with_slots: bool = False):
     """Token-interleaved layout: rank d holds tokens d, d + N, ...; a request's table entry
     jj * N + d names rank d's local page jj at a seeded random free slot.  Every rank gets the
-    same number of local pages, ceil(ceil(n / N) / 64).  Returns (req_page_ptr, dst_vpages)."""
+    same number of local pages, ceil(ceil(n / N) / 64).  Returns (req_page_ptr, dst_vpages), and
+    with ``with_slots`` also every entry's owner rank and pool slot (int64 CPU tensors)."""
     n_ranks = max(n_dcp, 1)
     local = [-(-(-(-int(n) // n_ranks)) // PAGE) for n in seq_lens]
     perms = [torch.randperm(slots_per_rank, generator=gen, device="cpu") for _ in range(n_ranks)]
     used = [0] * n_ranks
-    ptr, vp = [0], []
+    ptr, vp, owners, slots_of = [0], [], [], []
     for p in local:
         for jj in range(p):
             for d in range(n_ranks):
@@ -110,8 +118,13 @@ def token_page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Gener
                 slot = int(perms[d][used[d]])
                 used[d] += 1
                 vp.append(slot * n_ranks + d if n_dcp > 1 else slot)
+                owners.append(d)
+                slots_of.append(slot)
         ptr.append(ptr[-1] + p * n_ranks)
-    return torch.tensor(ptr, dtype=torch.int64), torch.tensor(vp, dtype=torch.int32)
+    out = (torch.tensor(ptr, dtype=torch.int64), torch.tensor(vp, dtype=torch.int32))
+    if with_slots:
+        out += (torch.tensor(owners, dtype=torch.int64), torch.tensor(slots_of, dtype=torch.int64))
+    return out
 
 
 @dataclass
@@ -132,6 +145,8 @@ class AttnCase:
     softmax_scale: float = SOFTMAX_SCALE
     name: str = ""
     layout: str = "page"            # "token": the table is token-interleaved (token_page_table)
+    page_owner: torch.Tensor | None = None  # int64 CPU [pages]: rank whose pool holds each entry
+    page_slot: torch.Tensor | None = None   # int64 CPU [pages]: that pool's slot
 
     @property
     def rows(self) -> int:
@@ -156,14 +171,15 @@ def attention_case(seq_lens, H: int, T: int, n_dcp: int, dtype: str, slots_per_r
     need = max(per_rank) if per_rank else 0
     if slots_per_rank is None:
         slots_per_rank = max(need, 1)
-    ptr, vp = page_table(seq_lens, n_dcp, slots_per_rank, gen_cpu)
+    ptr, vp, owner, slot = page_table(seq_lens, n_dcp, slots_per_rank, gen_cpu, with_slots=True)
     q = random_q(len(seq_lens), T, H, gen_dev, device)
     pools = [random_pool(slots_per_rank, dtype, gen_dev, device) for _ in range(n_ranks)]
     return AttnCase(B=len(seq_lens), T=T, H=H, n_dcp=n_dcp, dtype=dtype,
                     seq_lens=torch.tensor(seq_lens, dtype=torch.int32, device=device),
                     req_page_ptr=ptr.to(device), dst_vpages=vp.to(device), q=q, pools=pools,
                     slots_per_rank=slots_per_rank,
-                    kv_scale=FP8_KV_SCALE if dtype == "e4m3" else 1.0, name=name)
+                    kv_scale=FP8_KV_SCALE if dtype == "e4m3" else 1.0, name=name, page_owner=owner,
+                    page_slot=slot)
 
 
 @dataclass
@@ -183,6 +199,8 @@ class ReshardCase:
     dst_slots: int
     layer_counts: list = field(default_factory=list)
     name: str = ""
+    page_owner: torch.Tensor | None = None  # int64 CPU [pages]: destination rank of each entry
+    page_slot: torch.Tensor | None = None   # int64 CPU [pages]: its slot in that rank's pool
 
     @property
     def page_bytes(self) -> int:
@@ -197,13 +215,14 @@ def token_attention_case(seq_lens, H: int, T: int, n_dcp: int, dtype: str, seed:
     seq_lens = [int(n) for n in seq_lens]
     n_ranks = max(n_dcp, 1)
     slots = max(1, sum(-(-(-(-n // n_ranks)) // PAGE) for n in seq_lens))
-    ptr, vp = token_page_table(seq_lens, n_dcp, slots, gen_cpu)
+    ptr, vp, owner, slot = token_page_table(seq_lens, n_dcp, slots, gen_cpu, with_slots=True)
     q = random_q(len(seq_lens), T, H, gen_dev, device)
     pools = [random_pool(slots, dtype, gen_dev, device) for _ in range(n_ranks)]
     return AttnCase(B=len(seq_lens), T=T, H=H, n_dcp=n_dcp, dtype=dtype,
                     seq_lens=torch.tensor(seq_lens, dtype=torch.int32, device=device),
                     req_page_ptr=ptr.to(device), dst_vpages=vp.to(device), q=q, pools=pools, slots_per_rank=slots,
-                    kv_scale=FP8_KV_SCALE if dtype == "e4m3" else 1.0, name=name, layout="token")
+                    kv_scale=FP8_KV_SCALE if dtype == "e4m3" else 1.0, name=name, layout="token",
+                    page_owner=owner, page_slot=slot)
 
 
 SENTINEL_BYTE = 0xA5
@@ -226,7 +245,7 @@ def reshard_case(seq_lens, n_layers: int, layer_counts: list, n_dcp: int, dtype:
             per_rank[d] += (p - d + n_ranks - 1) // n_ranks if p > d else 0
     if dst_slots is None:
         dst_slots = max(max(per_rank), 1)
-    ptr, vp = page_table(seq_lens, n_dcp, dst_slots, gen_cpu)
+    ptr, vp, owner, slot = page_table(seq_lens, n_dcp, dst_slots, gen_cpu, with_slots=True)
     if src_pool_pages is None:
         src_pool_pages = max(total, 1)
     if contiguous_src:
@@ -243,7 +262,7 @@ def reshard_case(seq_lens, n_layers: int, layer_counts: list, n_dcp: int, dtype:
                        seq_lens=list(seq_lens), req_page_ptr=ptr.to(device),
                        src_pages=src.to(device), dst_vpages=vp.to(device), src_pools=src_pools,
                        src_pool_pages=src_pool_pages, dst_pools=dst_pools, dst_slots=dst_slots,
-                       layer_counts=list(layer_counts), name=name)
+                       layer_counts=list(layer_counts), name=name, page_owner=owner, page_slot=slot)
 
 
 def log_uniform_lengths(count: int, lo: int, hi: int, seed: int) -> list:
@@ -285,3 +304,15 @@ E2E_NCP = 4
 
 def e2e_lengths(seed: int = 4) -> list:
     return log_uniform_lengths(64, 2048, 500_000, seed)
+
+
+def e2e_layer_counts(layer_range) -> list:
+    """Layers held by each of the E2E_NCP source ranks under the caller's layer split."""
+    return [e - s for s, e in (layer_range(E2E_LAYERS, E2E_NCP, r) for r in range(E2E_NCP))]
+
+
+def e2e_reshard_case(device, layer_counts: list, seed: int = 1) -> ReshardCase:
+    """64 requests of 2K-500K tokens (log-uniform, multiples of 64), 8 layers, CP4 layer-split
+    source with each request's pages contiguous, DCP=8 destination, FP8-E4M3."""
+    return reshard_case(e2e_lengths(), n_layers=E2E_LAYERS, layer_counts=layer_counts, n_dcp=8, dtype="e4m3",
+                        contiguous_src=True, seed=seed, device=device, name="e2e-64x2K-500K-L8-cp4-dcp8-fp8")

@@ -38,6 +38,7 @@ DCP_KV_BF16 = 0
 DCP_KV_FP8_E4M3 = 1
 DEVERR_OUT_OF_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
+DEVERR_PLAN_MISMATCH = 0x4
 PAGE = 64
 K_DIM = 576
 V_DIM = 512
@@ -158,6 +159,33 @@ def _ptr_array(tensors, name) -> ctypes.Array:
     return (ctypes.c_void_p * len(tensors))(*[_dptr(t, f"{name}[{i}]") for i, t in enumerate(tensors)])
 
 
+def _check_pools(kv_pools) -> tuple[int, int]:
+    """Every pool [slots][64][576] of one dtype; returns (slots, dtype code)."""
+    if not kv_pools:
+        raise ValueError("kv_pools is empty")
+    slots = kv_pools[0].shape[0]
+    dtype = _kv_code(kv_pools[0])
+    for p in kv_pools:
+        if p.shape != (slots, PAGE, K_DIM) or p.dtype != kv_pools[0].dtype:
+            raise ValueError("every kv pool must be [slots][64][576] of one dtype")
+    return slots, dtype
+
+
+def _check_out(t: torch.Tensor | None, shape: tuple, name: str) -> None:
+    """A caller-supplied output must be fp32 of exactly this shape (the kernels write all of it)."""
+    if t is not None and (tuple(t.shape) != tuple(shape) or t.dtype != torch.float32):
+        raise ValueError(f"{name} must be float32 {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+
+
+def _pool_pages(t: torch.Tensor, name: str) -> tuple[int, int]:
+    """(layers, pages) of a pool [layers][pages][64][576] (or [pages][64][576] as one layer)."""
+    if t.dim() == 4 and tuple(t.shape[2:]) == (PAGE, K_DIM):
+        return t.shape[0], t.shape[1]
+    if t.dim() == 3 and tuple(t.shape[1:]) == (PAGE, K_DIM):
+        return 1, t.shape[0]
+    raise ValueError(f"{name} must be [layers][pages][64][576]")
+
+
 def device_error_status(word: int) -> int:
     return int(_load().dcp_device_error_status(int(word)))
 
@@ -271,6 +299,24 @@ def reshard_pages(req_page_ptr: torch.Tensor, src_pages: torch.Tensor, dst_vpage
     """Page-level reshard (all (r, d) paths in one launch); dst_pools are written in place."""
     dtype = _kv_code(src_pools[0])
     n_dcp = len(dst_pools) if n_dcp is None else n_dcp
+    if n_dcp > len(dst_pools):
+        raise ValueError(f"n_dcp = {n_dcp} but only {len(dst_pools)} destination pools")
+    n_cp = len(src_pools)
+    for r, p in enumerate(src_pools):
+        lay, pages = _pool_pages(p, f"src_pools[{r}]")
+        s0 = (num_layers // n_cp) * r + min(r, num_layers % n_cp)  # rank r's share of the layers
+        need = num_layers // n_cp + (1 if r < num_layers % n_cp else 0)
+        # the library addresses layer l of the pool at l * src_pool_pages pages
+        if (p.dtype != src_pools[0].dtype or lay < need or src_pool_pages > pages
+                or (need > 1 and src_pool_pages != pages)):
+            raise ValueError(f"src_pools[{r}] must be [{need}][src_pool_pages = {src_pool_pages}][64][576] "
+                             f"(layers from {s0}), got {tuple(p.shape)} {p.dtype}")
+    for d, p in enumerate(dst_pools[:n_dcp]):
+        lay, pages = _pool_pages(p, f"dst_pools[{d}]")
+        if (p.dtype != src_pools[0].dtype or lay < num_layers or dst_slots_per_rank > pages
+                or (num_layers > 1 and dst_slots_per_rank != pages)):
+            raise ValueError(f"dst_pools[{d}] must be [{num_layers}][dst_slots_per_rank = {dst_slots_per_rank}]"
+                             f"[64][576], got {tuple(p.shape)} {p.dtype}")
     sp = _ptr_array(src_pools, "src_pools")
     dp = _ptr_array(dst_pools, "dst_pools")
     _check(_load().dcp_reshard_pages(req_page_ptr.numel() - 1, _dptr(req_page_ptr, "req_page_ptr", torch.int64),
@@ -310,11 +356,9 @@ def partial_decode_attn(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: t
     if kd != K_DIM:
         raise ValueError("q must be [B][T][H][576]")
     N = len(kv_pools)
-    slots = kv_pools[0].shape[0]
-    dtype = _kv_code(kv_pools[0])
-    for p in kv_pools:
-        if p.shape != (slots, PAGE, K_DIM) or p.dtype != kv_pools[0].dtype:
-            raise ValueError("every kv pool must be [slots][64][576] of one dtype")
+    slots, dtype = _check_pools(kv_pools)
+    _check_out(o_part, (N, B, T, H, V_DIM), "o_part")
+    _check_out(lse_part, (N, B, T, H), "lse_part")
     dev = q.device
     if o_part is None:
         o_part = torch.empty((N, B, T, H, V_DIM), dtype=torch.float32, device=dev)
@@ -346,6 +390,7 @@ def attn_plan(q_shape: tuple, req_page_ptr: torch.Tensor, dst_vpages: torch.Tens
     """The attention's plan for this page table into ``workspace`` (dcp_attn_plan); q_shape =
     (B, T, H); kv_pools give the DCP size, slots per rank and dtype."""
     B, T, H = q_shape[:3]
+    _check_pools(kv_pools)
     _check(_load().dcp_attn_plan(B, T, H, _dptr(req_page_ptr, "req_page_ptr", torch.int64), dst_vpages.numel(),
                                  _dptr(dst_vpages, "dst_vpages", torch.int32), _kv_code(kv_pools[0]), len(kv_pools),
                                  kv_pools[0].shape[0], only_rank, _dptr(workspace, "workspace"), workspace.numel(),
@@ -371,16 +416,16 @@ def decode_attn_merged(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: to
     if kd != K_DIM:
         raise ValueError("q must be [B][T][H][576]")
     N = len(kv_pools)
-    slots = kv_pools[0].shape[0]
-    dtype = _kv_code(kv_pools[0])
-    for p in kv_pools:
-        if p.shape != (slots, PAGE, K_DIM) or p.dtype != kv_pools[0].dtype:
-            raise ValueError("every kv pool must be [slots][64][576] of one dtype")
+    slots, dtype = _check_pools(kv_pools)
+    _check_out(o_part, (N, B, T, H, V_DIM), "o_part")
+    _check_out(lse_part, (N, B, T, H), "lse_part")
     dev = q.device
     if o_part is None:
         o_part = torch.empty((N, B, T, H, V_DIM), dtype=torch.float32, device=dev)
     if lse_part is None:
         lse_part = torch.empty((N, B, T, H), dtype=torch.float32, device=dev)
+    _check_out(o_out, (B, T, H, V_DIM), "o_out")
+    _check_out(lse_out, (B, T, H), "lse_out")
     if o_out is None:
         o_out = torch.empty((B, T, H, V_DIM), dtype=torch.float32, device=dev)
     if lse_out is None:
@@ -418,8 +463,9 @@ def partial_decode_attn_static(q: torch.Tensor, seq_lens: torch.Tensor, req_page
     if kd != K_DIM:
         raise ValueError("q must be [B][T][H][576]")
     N = len(kv_pools)
-    slots = kv_pools[0].shape[0]
-    dtype = _kv_code(kv_pools[0])
+    slots, dtype = _check_pools(kv_pools)
+    _check_out(o_part, (N, B, T, H, V_DIM), "o_part")
+    _check_out(lse_part, (N, B, T, H), "lse_part")
     dev = q.device
     if o_part is None:
         o_part = torch.empty((N, B, T, H, V_DIM), dtype=torch.float32, device=dev)
@@ -447,6 +493,9 @@ def lse_merge(o_part: torch.Tensor, lse_part: torch.Tensor, o_out: torch.Tensor 
     rows = lse_part[0].numel()
     if o_part.numel() != n * rows * v:
         raise ValueError("o_part / lse_part shapes disagree")
+    for t, want, name in ((o_out, rows * v, "o_out"), (lse_out, rows, "lse_out")):
+        if t is not None and (t.numel() != want or t.dtype != torch.float32):
+            raise ValueError(f"{name} must be float32 with {want} elements")
     if o_out is None:
         o_out = torch.empty(o_part.shape[1:], dtype=torch.float32, device=o_part.device)
     if lse_out is None:

@@ -61,6 +61,7 @@ const char *dcp_status_string(int status) {
 int dcp_device_error_status(int32_t word) {
     if (word & DCP_DEVERR_TIMEOUT) return DCP_ERR_TIMEOUT;
     if (word & DCP_DEVERR_OUT_OF_RANGE) return DCP_ERR_OUT_OF_RANGE;
+    if (word & DCP_DEVERR_PLAN_MISMATCH) return DCP_ERR_WORKSPACE;
     return DCP_OK;
 }
 

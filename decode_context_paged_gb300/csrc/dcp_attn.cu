@@ -62,11 +62,6 @@ constexpr uint32_t kSCol = 256;          // S buffers start at TMEM column 256 (
 constexpr int kMaxTpc = 4096;
 
 constexpr float kPScale = 4.f;           // FP8 P is stored as 4 * p (p <= 2^6 under the lazy max)
-// FP8 P is split into E4M3 hi + lo terms unless the (rank, request) segment has at least this
-// many pages (8192 tokens).  One E4M3 term carries a relative rounding error of up to 2^-4 per
-// weight; its effect on O shrinks like 1/sqrt(effective number of keys), which for segments
-// this long stays far below the output tolerance, while short segments keep the lo term.
-constexpr int kSinglePMinPages = 128;
 
 #ifndef DCP_ATTN_S_BUFS_BF16
 #define DCP_ATTN_S_BUFS_BF16 3
@@ -109,18 +104,19 @@ struct Cfg {
 struct UnitInfo {
     int valid, d, b, g;
     int n_pages, out_index, limit, q_row0;
-    int rows_valid, p_single;  // p_single: FP8 P as one E4M3 term (no lo term)
+    int rows_valid;
     long long comp_base;
 };
 
 struct __align__(16) Ctl {
     float red[4][4][16];
-    float m_run[64];
+    float m_run[64];             // per query column: the reference maximum of the lazy softmax
     float corr[64];
     float oscale[64];
-    float qscale[64];            // per query row: softmax_scale * kappa * log2(e) * 2^-qexp
+    float qscale[64];            // per query column: softmax_scale * kappa * log2(e) (* 2^-qexp for FP8)
     uint64_t kfull[8], kempty[8];
     uint64_t vfull[kVSlots], vempty[kVSlots];
+    uint64_t vland;              // V units that need their tail rows cleared land here first
     uint64_t q_full, q_empty;
     uint64_t s_full[3], s_free[3];
     uint64_t p_full[2], o_done[2], o_free;  // p_full[t & 1]: P of global tile t written
@@ -145,7 +141,8 @@ struct KParams {
     const int32_t *comp_slot;  // [N][num_pages]: rank d's pages of request b start at d*num_pages + ptr[b]
     const int32_t *comp_page;  // page index j (within the request) of each compacted entry
     const int4 *units;         // {pair*G + g, page_begin, n_pages, out_index}
-    const int *ctrl;           // [0] = number of units, [1] = work counter
+    const int *ctrl;           // [0] = number of units, [1] = work counter; [3..7] the plan's key
+    unsigned long long plan_key;  // the key of this call's arguments (plan_key below)
     int *counter;
     const float *q_rscale;     // FP8: 2^-qexp per query row
     int B, T, H, HB, G, R;
@@ -228,6 +225,19 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
+// A plan stored in the workspace carries a key of the arguments it was made for (sizes, DCP
+// size, dtype, pool slots, rank selection, layout) and the page table's last CSR offset.  A run
+// whose own key or table differs, or a workspace that holds no plan, is refused on the device:
+// DCP_DEVERR_PLAN_MISMATCH, and no unit is run.
+constexpr int kPlanMagic = 0x44435031;  // "DCP1"
+
+__device__ __forceinline__ bool plan_matches(const int *ctrl, unsigned long long key, const int64_t *req_page_ptr,
+                                             int B) {
+    const unsigned long long k = *reinterpret_cast<const unsigned long long *>(ctrl + 4);
+    const long long last = *reinterpret_cast<const long long *>(ctrl + 6);
+    return ctrl[3] == kPlanMagic && k == key && last == (long long)req_page_ptr[B];
+}
+
 // Warp-uniform bounded wait: every lane polls, the warp agrees on the outcome.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           int32_t *err, uint64_t lim) {
@@ -238,13 +248,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
     __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&h);
-}
-
-// Four values to E4M3 (round to nearest even, saturating), packed little-endian.
-__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
-    const __nv_fp8x2_storage_t p01 = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-    const __nv_fp8x2_storage_t p23 = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-    return (uint32_t)p01 | ((uint32_t)p23 << 16);
 }
 
 // E4M3 hi/lo split of 4 values (already scaled into range): hi = e4m3(x), lo = e4m3(x - hi).
@@ -329,6 +332,7 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
             mbar_init(&ctl->vfull[i], 1);
             mbar_init(&ctl->vempty[i], 1);
         }
+        mbar_init(&ctl->vland, 1);
         mbar_init(&ctl->q_full, 1);
         mbar_init(&ctl->q_empty, 1);
         for (int i = 0; i < 3; ++i) {
@@ -360,7 +364,9 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
     grid_dep_wait();  // the plan (and the FP8 Q split) of this call
     grid_dep_launch();
     const uint32_t tmem = ctl->tmem_base;
-    const int n_units = p.ctrl[0];
+    const bool plan_ok = plan_matches(p.ctrl, p.plan_key, p.req_page_ptr, p.B);
+    if (!plan_ok && blockIdx.x == 0 && threadIdx.x == 0 && p.dev_error) atomicOr(p.dev_error, DCP_DEVERR_PLAN_MISMATCH);
+    const int n_units = plan_ok ? p.ctrl[0] : 0;
 
     // Consumer side of the unit ring (S issuer, V producer, PV issuer): returns false at the
     // end of the work or on abort.
@@ -372,10 +378,17 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
         ++k;
         return u.valid != 0;
     };
+    // Pool rows of a tile's two pages (a missing second page: a row past the pool, which the
+    // TMA fills with zeros).  The producers load them a tile ahead, off their critical path.
     auto tile_rows = [&](const UnitInfo &u, int tile, int &r0, int &r1) {
         const int pg = 2 * tile;
         r0 = p.comp_slot[u.comp_base + pg] * 64;
         r1 = (pg + 1 < u.n_pages) ? p.comp_slot[u.comp_base + pg + 1] * 64 : p.oob_row;
+    };
+    auto tile_pages = [&](const UnitInfo &u, int tile, int &ja, int &jb) {
+        const int pg = 2 * tile;
+        ja = p.comp_page[u.comp_base + pg];
+        jb = (pg + 1 < u.n_pages) ? p.comp_page[u.comp_base + pg + 1] : -1;
     };
 
     if (warp == 0) {
@@ -391,7 +404,7 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     ok = false;
                     break;
                 }
-                const int idx = atomicAdd(p.counter, 1);
+                const int idx = n_units > 0 ? atomicAdd(p.counter, 1) : 0;  // (no plan: no workspace write)
                 UnitInfo u;
                 u.valid = idx < n_units;
                 if (u.valid) {
@@ -401,8 +414,7 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     u.d = pair / p.B;
                     u.b = pair - u.d * p.B;
                     const int t = u.g / p.HB, hb = u.g - (u.g / p.HB) * p.HB;
-                    u.n_pages = rec.z & 0x3FFFFFFF;
-                    u.p_single = (rec.z >> 30) & 1;
+                    u.n_pages = rec.z;
                     u.out_index = rec.w;
                     u.limit = p.seq_lens[u.b] - p.T + t;
                     u.q_row0 = (u.b * p.T + t) * p.H + hb * kGroupRows;
@@ -433,9 +445,11 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                         tma_load_2d(sq + kb * 8192, &maps.q[0], &ctl->q_full, kb * 64, u.q_row0);
                 }
                 const CUtensorMap *km = maps.kv[u.d];
+                int rn0, rn1;
+                tile_rows(u, 0, rn0, rn1);
                 for (int i = 0; i < nt && ok; ++i) {
-                    int r0, r1;
-                    tile_rows(u, i, r0, r1);
+                    const int r0 = rn0, r1 = rn1;
+                    if (i + 1 < nt) tile_rows(u, i + 1, rn0, rn1);
                     for (int kb = 0; kb < C::kKBlocks; ++kb) {
                         const uint32_t slot = kpos % kKSlots;
                         if (!mbar_wait(&ctl->kempty[slot], ((kpos / kKSlots) & 1) ^ 1, abort_flag, p.dev_error, lim)) {
@@ -457,10 +471,11 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     }
                 }
             }
-            if (!ok) {  // let issued TMA copies land before the CTA can exit
-                const uint64_t t0 = global_timer_ns();
-                while (global_timer_ns() - t0 < 200000ull) {
-                }
+            if (!ok) {  // let issued TMA copies land before the CTA can exit (bounded waits)
+                int never = 0;
+                for (uint32_t q = kpos > (uint32_t)kKSlots ? kpos - kKSlots : 0; q < kpos; ++q)
+                    mbar_wait(&ctl->kfull[q % kKSlots], (q / kKSlots) & 1, &never, nullptr, lim);
+                if (q_cnt > 0) mbar_wait(&ctl->q_full, (q_cnt - 1) & 1, &never, nullptr, lim);
             }
         }
     } else if (warp == 1) {
@@ -530,17 +545,43 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
         }
     } else if (warp == 2) {
         // ---------------------------------------------------------------- V-stream TMA
+        // Rows of a page past the request's length hold no key and may hold any bytes (NaN
+        // included): P is zero there, but 0 x NaN would reach O, so a V unit with such rows
+        // lands on vland first, the rows are cleared, and only then is vfull released.
         if (lane == 0) {
             const uint64_t pol = make_policy_evict_first();
-            uint32_t vpos = 0, k = 0;
-            bool ok = true;
+            uint32_t vpos = 0, k = 0, land_cnt = 0;
+            bool ok = true, land_pending = false;
+            uint32_t via_land = 0;  // bit per slot: its latest unit went through vland
             UnitInfo u;
+            // rows of the page with index j (within the request) that hold positions < seq
+            auto valid_rows = [&](int j, int seq) -> int {
+                long long nv;
+                if (p.tok_n == 0) {
+                    nv = (long long)seq - 64LL * j;
+                } else {
+                    const int c = j % p.tok_n;
+                    nv = seq > c ? ((long long)seq - c + p.tok_n - 1) / p.tok_n - 64LL * (j / p.tok_n) : 0;
+                }
+                return (int)(nv < 0 ? 0 : nv > 64 ? 64 : nv);
+            };
             while (ok && next_unit(k, u)) {
                 const int nt = (u.n_pages + 1) >> 1;
                 const CUtensorMap *km = &maps.kv[u.d][0];
+                if (nt == 0) continue;
+                const int seq = p.seq_lens[u.b];
+                int rn0, rn1, jn0, jn1;
+                tile_rows(u, 0, rn0, rn1);
+                tile_pages(u, 0, jn0, jn1);
                 for (int i = 0; i < nt && ok; ++i) {
-                    int r0, r1;
-                    tile_rows(u, i, r0, r1);
+                    const int r0 = rn0, r1 = rn1;
+                    const int nv0 = valid_rows(jn0, seq);
+                    const int nv1 = jn1 >= 0 ? valid_rows(jn1, seq) : 64;  // a missing page is zero-filled
+                    if (i + 1 < nt) {
+                        tile_rows(u, i + 1, rn0, rn1);
+                        tile_pages(u, i + 1, jn0, jn1);
+                    }
+                    const bool fix = nv0 < 64 || nv1 < 64;
                     for (int vu = 0; vu < C::kVUnits; ++vu) {
                         const uint32_t slot = vpos % kVSlots;
                         if (!mbar_wait(&ctl->vempty[slot], ((vpos / kVSlots) & 1) ^ 1, abort_flag, p.dev_error, lim)) {
@@ -549,21 +590,44 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                         }
                         ++vpos;
                         uint8_t *dst = vring + slot * kVSlotBytes;
-                        mbar_arrive_expect_tx(&ctl->vfull[slot], kVSlotBytes);
+                        uint64_t *bar = fix ? &ctl->vland : &ctl->vfull[slot];
+                        via_land = fix ? (via_land | (1u << slot)) : (via_land & ~(1u << slot));
+                        land_pending = fix;
+                        mbar_arrive_expect_tx(bar, kVSlotBytes);
                         const int w = F8 ? 128 : 64;  // dims per block
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const int x = (2 * vu + h) * w;
-                            tma_load_2d_hint(dst + h * 16384, km, &ctl->vfull[slot], x, r0, pol);
-                            tma_load_2d_hint(dst + h * 16384 + 8192, km, &ctl->vfull[slot], x, r1, pol);
+                            tma_load_2d_hint(dst + h * 16384, km, bar, x, r0, pol);
+                            tma_load_2d_hint(dst + h * 16384 + 8192, km, bar, x, r1, pol);
+                        }
+                        if (fix) {
+                            if (!mbar_wait(&ctl->vland, land_cnt & 1, abort_flag, p.dev_error, lim)) {
+                                ok = false;
+                                break;
+                            }
+                            ++land_cnt;
+                            land_pending = false;
+                            // a row of one 64-dim (BF16) or 128-dim (E4M3) block is 128 contiguous
+                            // bytes whatever the swizzle: clear rows [nv, 64) of each page
+#pragma unroll 1
+                            for (int h = 0; h < 2; ++h)
+#pragma unroll 1
+                                for (int pg = 0; pg < 2; ++pg) {
+                                    uint4 *row = reinterpret_cast<uint4 *>(dst + h * 16384 + pg * 8192);
+                                    for (int e = (pg ? nv1 : nv0) * 8; e < 64 * 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
+                                }
+                            fence_proxy_async_smem();
+                            mbar_arrive(&ctl->vfull[slot]);
                         }
                     }
                 }
             }
-            if (!ok) {
-                const uint64_t t0 = global_timer_ns();
-                while (global_timer_ns() - t0 < 200000ull) {
-                }
+            if (!ok) {  // let issued TMA copies land before the CTA can exit (bounded waits)
+                int never = 0;
+                for (uint32_t q = vpos > (uint32_t)kVSlots ? vpos - kVSlots : 0; q < vpos; ++q)
+                    if (!((via_land >> (q % kVSlots)) & 1u)) mbar_wait(&ctl->vfull[q % kVSlots], (q / kVSlots) & 1, &never, nullptr, lim);
+                if (land_pending) mbar_wait(&ctl->vland, land_cnt & 1, &never, nullptr, lim);
             }
         }
     } else if (warp == 3) {
@@ -609,9 +673,8 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                                     const uint64_t ad = smem_desc(a0 + h * 16384 + kk * 4096, 16384, 1024, kSwizzle128);
                                     mma_f8_ss(d_tmem, ad, smem_desc(pb + kk * 2048, 512, 512, kSwizzle64),
                                               C::kIdescPV, !(i == 0 && kk == 0));
-                                    if (!u.p_single)
-                                        mma_f8_ss(d_tmem, ad, smem_desc(pb + 8192 + kk * 2048, 512, 512, kSwizzle64),
-                                                  C::kIdescPV, 1);
+                                    mma_f8_ss(d_tmem, ad, smem_desc(pb + 8192 + kk * 2048, 512, 512, kSwizzle64),
+                                              C::kIdescPV, 1);
                                 }
                             }
                         } else {
@@ -660,6 +723,21 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
             int fail = !warp_wait(&ctl->unit_full[e], (k >> 1) & 1, abort_flag, p.dev_error, lim);
             if (named_bar_or(bar_a, 128, fail)) break;
             const UnitInfo u = ctl->unit[e];
+            // Per-column score scale and reference maximum, in shared memory (read back as
+            // vectors each tile; registers stay free for the scores).  The reference trails the
+            // true running maximum by at most kLazyTau (log2 units): a tile whose scores all
+            // stay within that margin is exponentiated against the old reference (weights up to
+            // 2^kLazyTau, exact after the final normalisation) and skips the cross-thread
+            // maximum and the O rescale.
+            if (u.valid && gtid < kCols) {
+                float qs = p.sl2;
+                if (F8) {
+                    const int qr = u.q_row0 + c0 + gtid;
+                    qs *= (qr < p.R) ? __ldg(p.q_rscale + qr) : 0.f;
+                }
+                ctl->qscale[c0 + gtid] = qs;
+                ctl->m_run[c0 + gtid] = -INFINITY;
+            }
             named_bar_sync(bar_b, 128);
             if (gtid == 0) mbar_arrive(&ctl->unit_empty[e]);
             ++k;
@@ -680,24 +758,11 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                 if (gtid < kCols && c0 + gtid < u.rows_valid) lbase[out_row0 + c0 + gtid] = -INFINITY;
                 continue;
             }
-            // Per-column score scale and reference maximum, kept in registers.  The reference
-            // trails the true running maximum by at most kLazyTau (log2 units): a tile whose
-            // scores all stay within that margin is exponentiated against the old reference
-            // (weights up to 2^kLazyTau, exact after the final normalisation) and skips the
-            // cross-thread maximum and the O rescale.
-            float qsr[kCols], mref[kCols], lp[kCols];
+            float lp[kCols];
 #pragma unroll
-            for (int c = 0; c < kCols; ++c) {
-                float qs = p.sl2;
-                if (F8) {
-                    const int qr = u.q_row0 + c0 + c;
-                    qs *= (qr < p.R) ? __ldg(p.q_rscale + qr) : 0.f;
-                }
-                qsr[c] = qs;
-                mref[c] = -INFINITY;
-                lp[c] = 0.f;
-            }
-            if (gtid < kCols) ctl->m_run[c0 + gtid] = -INFINITY;
+            for (int c = 0; c < kCols; ++c) lp[c] = 0.f;
+            const float4 *qs4 = reinterpret_cast<const float4 *>(&ctl->qscale[c0]);
+            const float4 *mr4 = reinterpret_cast<const float4 *>(&ctl->m_run[c0]);
             // page index of this row's page in tile 0, then prefetched one tile ahead
             int j_cur = -1;
             {
@@ -739,9 +804,15 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                         : ((long long)(j_cur / p.tok_n) * 64 + (row & 63)) * p.tok_n + (j_cur % p.tok_n);
                     const bool valid = j_cur >= 0 && pos <= (long long)u.limit;
 #pragma unroll
-                    for (int c = 0; c < kCols; ++c) {
-                        s[c] = valid ? s[c] * qsr[c] : -INFINITY;
-                        over |= s[c] > mref[c] + kLazyTau;
+                    for (int q = 0; q < kCols / 4; ++q) {
+                        const float4 a = qs4[q], m = mr4[q];
+                        const float av[4] = {a.x, a.y, a.z, a.w}, mv[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const int c = 4 * q + k;
+                            s[c] = valid ? s[c] * av[k] : -INFINITY;
+                            over |= s[c] > mv[k] + kLazyTau;
+                        }
                     }
                 }
                 j_cur = j_next;
@@ -767,7 +838,6 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     float cr[kCols];
 #pragma unroll
                     for (int c = 0; c < kCols; ++c) {
-                        mref[c] = ctl->m_run[c0 + c];
                         cr[c] = ctl->corr[c0 + c];
                         lp[c] *= cr[c];
                     }
@@ -797,10 +867,16 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     tc_fence_after();
                 }
 #pragma unroll
-                for (int c = 0; c < kCols; ++c) {
-                    const float ms = mref[c] == -INFINITY ? 0.f : mref[c];
-                    s[c] = fast_exp2(s[c] - ms);
-                    lp[c] += s[c];
+                for (int q = 0; q < kCols / 4; ++q) {
+                    const float4 m = mr4[q];
+                    const float mv[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int c = 4 * q + k;
+                        const float ms = mv[k] == -INFINITY ? 0.f : mv[k];
+                        s[c] = fast_exp2(s[c] - ms);
+                        lp[c] += s[c];
+                    }
                 }
                 if (F8) {
                     // P^T row as hi and lo E4M3 rows of 64 bytes, MN-major, 64-byte swizzle;
@@ -808,22 +884,13 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     const uint32_t off = (row >> 3) * 512 + (row & 7) * 64;
                     const uint32_t sw = ((wg ^ ((row >> 1) & 3)) << 4);
                     uint8_t *pbuf = sp + (g % C::kPBufs) * kPBytes;
-                    if (u.p_single) {
-                        uint4 hv;
-                        hv.x = e4m3x4(s[0] * kPScale, s[1] * kPScale, s[2] * kPScale, s[3] * kPScale);
-                        hv.y = e4m3x4(s[4] * kPScale, s[5] * kPScale, s[6] * kPScale, s[7] * kPScale);
-                        hv.z = e4m3x4(s[8] * kPScale, s[9] * kPScale, s[10] * kPScale, s[11] * kPScale);
-                        hv.w = e4m3x4(s[12] * kPScale, s[13] * kPScale, s[14] * kPScale, s[15] * kPScale);
-                        *reinterpret_cast<uint4 *>(pbuf + off + sw) = hv;
-                    } else {
-                        uint4 hv, lv;
-                        split_e4m3x4(s[0] * kPScale, s[1] * kPScale, s[2] * kPScale, s[3] * kPScale, hv.x, lv.x);
-                        split_e4m3x4(s[4] * kPScale, s[5] * kPScale, s[6] * kPScale, s[7] * kPScale, hv.y, lv.y);
-                        split_e4m3x4(s[8] * kPScale, s[9] * kPScale, s[10] * kPScale, s[11] * kPScale, hv.z, lv.z);
-                        split_e4m3x4(s[12] * kPScale, s[13] * kPScale, s[14] * kPScale, s[15] * kPScale, hv.w, lv.w);
-                        *reinterpret_cast<uint4 *>(pbuf + off + sw) = hv;
-                        *reinterpret_cast<uint4 *>(pbuf + 8192 + off + sw) = lv;
-                    }
+                    uint4 hv, lv;
+                    split_e4m3x4(s[0] * kPScale, s[1] * kPScale, s[2] * kPScale, s[3] * kPScale, hv.x, lv.x);
+                    split_e4m3x4(s[4] * kPScale, s[5] * kPScale, s[6] * kPScale, s[7] * kPScale, hv.y, lv.y);
+                    split_e4m3x4(s[8] * kPScale, s[9] * kPScale, s[10] * kPScale, s[11] * kPScale, hv.z, lv.z);
+                    split_e4m3x4(s[12] * kPScale, s[13] * kPScale, s[14] * kPScale, s[15] * kPScale, hv.w, lv.w);
+                    *reinterpret_cast<uint4 *>(pbuf + off + sw) = hv;
+                    *reinterpret_cast<uint4 *>(pbuf + 8192 + off + sw) = lv;
                 } else {
                     // P^T row: 64 BF16 values, MN-major with the 128-byte swizzle; this
                     // warpgroup writes 16-byte chunks 2wg and 2wg + 1.
@@ -911,10 +978,13 @@ __global__ void __launch_bounds__(kPlanThreads)
 plan_count_kernel(int N, long long slots_per_rank, int tiles_per_req, int tile_stride, int n_tile_blocks,
                   const int64_t *__restrict__ req_page_ptr, const int32_t *__restrict__ vpages,
                   int32_t *__restrict__ tile_cnt, int32_t *dev_error, int R, const __nv_bfloat16 *__restrict__ q,
-                  uint8_t *__restrict__ qhl, float *__restrict__ rscale) {
+                  uint8_t *__restrict__ qhl, float *__restrict__ rscale, const int *__restrict__ run_ctrl,
+                  unsigned long long key, int B) {
     grid_dep_wait();
     grid_dep_launch();
     if ((int)blockIdx.x >= n_tile_blocks) {  // FP8 Q split: one warp per query row
+        // a run of a stored plan (run_ctrl set) writes nothing when the workspace holds no plan for it
+        if (run_ctrl && !plan_matches(run_ctrl, key, req_page_ptr, B)) return;
         const int row = ((int)blockIdx.x - n_tile_blocks) * (kPlanThreads / 32) + (int)(threadIdx.x >> 5);
         if (row < R) q_split_row(row, R, q, qhl, rscale);
         return;
@@ -1020,7 +1090,8 @@ __device__ void plan_scatter_tile(int b, int k, int N, long long num_pages, long
 // The last block of plan_build_kernel: chunk each (rank, request) pair, assign partial slots,
 // list the multi-chunk pairs, emit units largest first with the G query groups of a chunk
 // adjacent.
-__device__ void plan_build_units(int B, int N, int G, int only_rank, int tpc, const int64_t *__restrict__ req_page_ptr,
+__device__ void plan_build_units(int B, int N, int G, int only_rank, int tpc, unsigned long long key,
+                                 const int64_t *__restrict__ req_page_ptr,
                                  int tiles_per_req, const int32_t *__restrict__ tile_cnt, int32_t *__restrict__ counts,
                                  int32_t *__restrict__ pair_chunks, int32_t *__restrict__ pair_part,
                                  int32_t *__restrict__ multi_list, int4 *__restrict__ units, int *__restrict__ ctrl) {
@@ -1073,6 +1144,9 @@ __device__ void plan_build_units(int B, int N, int G, int only_rank, int tpc, co
         ctrl[0] = acc * G;
         ctrl[1] = 0;
         ctrl[2] = n_multi;
+        ctrl[3] = kPlanMagic;
+        *reinterpret_cast<unsigned long long *>(ctrl + 4) = key;
+        *reinterpret_cast<long long *>(ctrl + 6) = (long long)req_page_ptr[B];
     }
     __syncthreads();
     for (int pr = threadIdx.x; pr < n_pair; pr += blockDim.x) {
@@ -1088,15 +1162,15 @@ __device__ void plan_build_units(int B, int N, int G, int only_rank, int tpc, co
             for (int g = 0; g < G; ++g) {
                 const int out = chunks > 1 ? pair_part[pr] + c * G + g : -1;
                 units[(long long)slot * G + g] =
-                    make_int4(pr * G + g, page_begin,
-                              n_pages | (cnt >= kSinglePMinPages ? (1 << 30) : 0), out);
+                    make_int4(pr * G + g, page_begin, n_pages, out);
             }
         }
     }
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
-plan_build_kernel(int B, int N, int G, int only_rank, int tpc, long long num_pages, long long slots_per_rank,
+plan_build_kernel(int B, int N, int G, int only_rank, int tpc, unsigned long long key, long long num_pages,
+                  long long slots_per_rank,
                   int tiles_per_req, int tile_stride, const int64_t *__restrict__ req_page_ptr, const int32_t *__restrict__ vpages,
                   const int32_t *__restrict__ tile_cnt, int32_t *__restrict__ comp_slot, int32_t *__restrict__ comp_page,
                   int32_t *__restrict__ counts, int32_t *__restrict__ pair_chunks, int32_t *__restrict__ pair_part,
@@ -1111,18 +1185,20 @@ plan_build_kernel(int B, int N, int G, int only_rank, int tpc, long long num_pag
             plan_scatter_tile(b, k, N, num_pages, slots_per_rank, tiles_per_req, req_page_ptr, vpages, tile_cnt,
                               comp_slot, comp_page);
     } else
-        plan_build_units(B, N, G, only_rank, tpc, req_page_ptr, tiles_per_req, tile_cnt, counts, pair_chunks,
+        plan_build_units(B, N, G, only_rank, tpc, key, req_page_ptr, tiles_per_req, tile_cnt, counts, pair_chunks,
                          pair_part, multi_list, units, ctrl);
 }
 
 // Merge the chunk partials of the multi-chunk (rank, request) pairs listed by the plan into
 // O_part / LSE_part; a grid-stride loop over (listed pair, query group, row), one warp each.
-__global__ void combine_kernel(int B, int T, int H, int HB, int G, int *ctrl,
+__global__ void combine_kernel(int B, int T, int H, int HB, int G, int *ctrl, unsigned long long key,
+                               const int64_t *__restrict__ req_page_ptr,
                                const int32_t *__restrict__ multi_list, const int32_t *__restrict__ pair_chunks,
                                const int32_t *__restrict__ pair_part, const float *part_o, const float *part_lse,
                                float *o_part, float *lse_part) {
     grid_dep_wait();
     grid_dep_launch();
+    if (!plan_matches(ctrl, key, req_page_ptr, B)) return;
     if (blockIdx.x == 0 && threadIdx.x == 0) ctrl[1] = 0;  // the work counter, ready for the next run of the plan
     const long long n_tasks = (long long)ctrl[2] * G * kGroupRows;
     const int wpb = blockDim.x >> 5;
@@ -1148,13 +1224,15 @@ __global__ void combine_kernel(int B, int T, int H, int HB, int G, int *ctrl,
 // Fused merge, first launch after the attention kernel.  With no multi-chunk pair (ctrl[2] ==
 // 0) it merges every row over the ranks, one warp per row, ascending rank order.  Otherwise it combines the chunk partials as combine_kernel does
 // and leaves the rank merge to merge_after_combine_kernel.
-__global__ void merge_combine_kernel(int B, int T, int H, int HB, int G, int N, int *ctrl,
+__global__ void merge_combine_kernel(int B, int T, int H, int HB, int G, int N, int *ctrl, unsigned long long key,
+                                     const int64_t *__restrict__ req_page_ptr,
                                      const int32_t *__restrict__ multi_list, const int32_t *__restrict__ pair_chunks,
                                      const int32_t *__restrict__ pair_part, const float *part_o,
                                      const float *part_lse, float *o_part, float *lse_part, float *o_out,
                                      float *lse_out) {
     grid_dep_wait();
     grid_dep_launch();
+    if (!plan_matches(ctrl, key, req_page_ptr, B)) return;
     if (blockIdx.x == 0 && threadIdx.x == 0) ctrl[1] = 0;  // the work counter, ready for the next run of the plan
     const int n_multi = ctrl[2];
     const int wpb = blockDim.x >> 5;
@@ -1185,11 +1263,12 @@ __global__ void merge_combine_kernel(int B, int T, int H, int HB, int G, int N, 
 
 // Fused merge, second launch: the rank merge of every row when merge_combine_kernel combined
 // chunk partials instead (ctrl[2] > 0); exits at once otherwise.
-__global__ void merge_after_combine_kernel(int N, long long rows, const int *__restrict__ ctrl, const float *o_part,
+__global__ void merge_after_combine_kernel(int N, long long rows, const int *__restrict__ ctrl, unsigned long long key,
+                                           const int64_t *__restrict__ req_page_ptr, int B, const float *o_part,
                                            const float *lse_part, float *o_out, float *lse_out) {
     grid_dep_wait();
     grid_dep_launch();
-    if (ctrl[2] == 0) return;
+    if (!plan_matches(ctrl, key, req_page_ptr, B) || ctrl[2] == 0) return;
     const int wpb = blockDim.x >> 5;
     for (long long row = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * wpb)
         warp_merge_row512(N, o_part + row * kVDim, rows * kVDim, lse_part + row, rows, o_out + row * kVDim,
@@ -1231,6 +1310,21 @@ bool make_map(CUtensorMap *m, const void *ptr, uint64_t rows, bool bf16, uint32_
 }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Key of the arguments a plan depends on (splitmix64 steps over the fields).
+unsigned long long plan_key(const AttnPlanShape &s, int dtype, int only_rank, int64_t slots_per_rank,
+                            int token_layout) {
+    const long long f[9] = {s.B, s.T, s.H, s.N, dtype, only_rank, (long long)slots_per_rank, (long long)s.num_pages,
+                            token_layout};
+    unsigned long long h = 0x9E3779B97F4A7C15ull;
+    for (long long v : f) {
+        h ^= (unsigned long long)v + 0x9E3779B97F4A7C15ull + (h << 6) + (h >> 2);
+        h = (h ^ (h >> 30)) * 0xBF58476D1CE4E5B9ull;
+        h = (h ^ (h >> 27)) * 0x94D049BB133111EBull;
+        h ^= h >> 31;
+    }
+    return h;
+}
 
 }  // namespace
 
@@ -1293,7 +1387,7 @@ bool plan_attention(int B, int T, int H, int N, int64_t num_pages, int dtype, in
     s->off_units = off;   off = align256(off + sizeof(int4) * (size_t)s->max_units);
     s->off_seg = off;     off = align256(off + sizeof(int32_t) * 2 * (size_t)N * B);
     s->off_multi = off;   off = align256(off + sizeof(int32_t) * (size_t)N * B);
-    s->off_ctrl = off;    off = align256(off + sizeof(int32_t) * 4);
+    s->off_ctrl = off;    off = align256(off + sizeof(int32_t) * 8);
     s->tiles_per_req = (int)std::max<long long>(1, (num_pages + kPlanTile - 1) / kPlanTile);
     s->off_tiles = off;   off = align256(off + sizeof(int32_t) * (size_t)B * s->tiles_per_req * kMaxDcpAttn);
     s->off_part_o = off;  off = align256(off + sizeof(float) * (size_t)s->max_partials * kGroupRows * kVDim);
@@ -1334,6 +1428,7 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
 
     int32_t *tile_cnt = reinterpret_cast<int32_t *>(ws + s.off_tiles);
     int32_t *multi_list = reinterpret_cast<int32_t *>(ws + s.off_multi);
+    const unsigned long long key = plan_key(s, a.dtype, a.only_rank, a.slots_per_rank, a.token_layout);
     // blocks per request: about three blocks per SM in all, at most one per tile
     const int tile_stride = (int)std::max<long long>(
         1, std::min<long long>(s.tiles_per_req, (3LL * num_sms + s.B - 1) / s.B));
@@ -1343,11 +1438,12 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     if (n_tile_blocks + q_blocks > 0 &&
         launch_pdl(plan_count_kernel, dim3(n_tile_blocks + q_blocks), dim3(kPlanThreads), 0, stream, s.N,
                    (long long)a.slots_per_rank, s.tiles_per_req, tile_stride, n_tile_blocks, a.req_page_ptr, a.dst_vpages, tile_cnt,
-                   a.dev_error, R, reinterpret_cast<const __nv_bfloat16 *>(a.q), qhl, qscale) != cudaSuccess)
+                   a.dev_error, R, reinterpret_cast<const __nv_bfloat16 *>(a.q), qhl, qscale,
+                   a.phase == 2 ? (const int *)ctrl : nullptr, key, s.B) != cudaSuccess)
         return DCP_ERR_CUDA;
     if (a.phase != 2 &&
         launch_pdl(plan_build_kernel, dim3(n_tile_blocks + 1), dim3(kPlanThreads), 0, stream, s.B, s.N, s.G,
-                   a.only_rank, s.tiles_per_chunk, (long long)s.num_pages, (long long)a.slots_per_rank, s.tiles_per_req,
+                   a.only_rank, s.tiles_per_chunk, key, (long long)s.num_pages, (long long)a.slots_per_rank, s.tiles_per_req,
                    tile_stride, a.req_page_ptr, a.dst_vpages, (const int32_t *)tile_cnt, comp_slot, comp_page, counts, pair_chunks,
                    pair_part, multi_list, units, ctrl) != cudaSuccess)
         return DCP_ERR_CUDA;
@@ -1375,6 +1471,7 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     kp.comp_page = comp_page;
     kp.units = units;
     kp.ctrl = ctrl;
+    kp.plan_key = key;
     kp.counter = ctrl + 1;
     kp.q_rscale = qscale;
     kp.B = s.B;
@@ -1403,13 +1500,13 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
         const long long tasks = std::max<long long>(rows, (long long)s.N * s.B * s.G * kGroupRows);
         const int blocks = (int)std::max<long long>(1, std::min<long long>((tasks + 7) / 8, 8LL * num_sms));
         if (launch_pdl(merge_combine_kernel, dim3(blocks), dim3(256), 0, stream, s.B, s.T, s.H, kp.HB, s.G, s.N,
-                       ctrl, (const int32_t *)multi_list, (const int32_t *)pair_chunks,
+                       ctrl, key, a.req_page_ptr, (const int32_t *)multi_list, (const int32_t *)pair_chunks,
                        (const int32_t *)pair_part, (const float *)part_o, (const float *)part_lse, a.o_part,
                        a.lse_part, a.o_out, a.lse_out) != cudaSuccess)
             return DCP_ERR_CUDA;
         const int mblocks = (int)std::max<long long>(1, std::min<long long>((rows + 7) / 8, 8LL * num_sms));
         if (launch_pdl(merge_after_combine_kernel, dim3(mblocks), dim3(256), 0, stream, s.N, rows,
-                       (const int *)ctrl, (const float *)a.o_part, (const float *)a.lse_part, a.o_out,
+                       (const int *)ctrl, key, a.req_page_ptr, s.B, (const float *)a.o_part, (const float *)a.lse_part, a.o_out,
                        a.lse_out) != cudaSuccess)
             return DCP_ERR_CUDA;
         return DCP_OK;
@@ -1418,7 +1515,7 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     const long long max_tasks = (long long)s.N * s.B * s.G * kGroupRows;
     const int combine_blocks = (int)std::max<long long>(1, std::min<long long>((max_tasks + 7) / 8, 8LL * num_sms));
     if (launch_pdl(combine_kernel, dim3(combine_blocks), dim3(256), 0, stream, s.B, s.T, s.H, kp.HB, s.G,
-                   ctrl, (const int32_t *)multi_list, (const int32_t *)pair_chunks,
+                   ctrl, key, a.req_page_ptr, (const int32_t *)multi_list, (const int32_t *)pair_chunks,
                    (const int32_t *)pair_part, (const float *)part_o, (const float *)part_lse, a.o_part,
                    a.lse_part) != cudaSuccess)
         return DCP_ERR_CUDA;

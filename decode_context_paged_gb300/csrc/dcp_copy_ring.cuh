@@ -67,10 +67,11 @@ __device__ bool copy_ring(int64_t c_begin, int64_t c_end, Map map, uint8_t *smem
     while (ok && stored < issued) ok = store_one();
     bulk_wait<0>();
     if (!ok) {
-        // A load wait gave up: let the copies already issued land before the CTA exits.
-        const uint64_t t0 = global_timer_ns();
-        while (global_timer_ns() - t0 < 200000ull) {
-        }
+        // A load wait gave up: let the loads already issued (chunks stored..issued-1) land before
+        // the CTA exits, each with a bounded wait of its own.
+        int never = 0;
+        for (int64_t c = stored; c < issued; ++c)
+            mbar_wait(&bars[c % kRingStages], (uint32_t)((c / kRingStages) & 1), &never, nullptr, wait_limit_ns);
     }
     return ok;
 }

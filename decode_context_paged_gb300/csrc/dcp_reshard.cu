@@ -7,12 +7,15 @@
 //   value, source indices pass through), 6.4 (the copy unit is the physical 64-token page).
 //
 // The reshard is a pure HBM->HBM byte move: every (layer, page) item is one contiguous page
-// read and one contiguous page written.  One CTA per SM runs a single issuing thread that
-// streams 18 KB chunks through an 11-stage shared-memory ring with TMA bulk copies
-// (cp.async.bulk global->shared completing on an mbarrier, then shared->global in bulk
-// groups), keeping ~8 loads and ~3 stores in flight per SM.  Work is split as contiguous
-// chunk ranges of the flattened (layer, page, chunk) space; all (r, d) paths share the launch.
+// read and one contiguous page written.  Each CTA runs a single issuing thread that streams
+// 36 KB chunks through a 6-stage shared-memory ring with TMA bulk copies (cp.async.bulk
+// global->shared completing on an mbarrier, then shared->global in bulk groups), 3 loads ahead
+// of the stores (copy_ring in dcp_copy_ring.cuh).  The grid is one CTA per SM for short copies
+// and one per pair of SMs for long ones (ring_ctas below).  Work is split as contiguous chunk
+// ranges of the flattened (layer, page, chunk) space; all (r, d) paths share the launch.
 #include <cuda_runtime.h>
+
+#include <cstdlib>
 
 #include "dcp_copy_ring.cuh"
 #include "dcp_internal.h"
@@ -307,7 +310,14 @@ filter_kernel(int64_t n, const int32_t *__restrict__ dst_vpages,
 // queueing rather than bandwidth).  Short copies keep one CTA per SM: on a 0.6 GB reshard inside
 // a decode step, 152 CTAs are 1-2% faster (the shorter ramp counts more).  The switch sits at
 // 16 MB per CTA of the half grid.
+// DCP_RING_CTAS (environment, a positive count) overrides the choice; the tests use it to run
+// the copy kernels on grids of other sizes.
 inline int ring_ctas(int num_sms, int64_t bytes) {
+    const char *e = std::getenv("DCP_RING_CTAS");
+    if (e && *e) {
+        const long v = std::strtol(e, nullptr, 10);
+        if (v > 0) return (int)(v < 65535 ? v : 65535);
+    }
     const int half = num_sms > 1 ? num_sms / 2 : 1;
     return bytes >= (int64_t)half * (16ll << 20) ? half : num_sms;
 }

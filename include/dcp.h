@@ -71,6 +71,8 @@ typedef enum { DCP_KV_BF16 = 0, DCP_KV_FP8_E4M3 = 1 } dcp_kv_dtype;
 /* Bits OR-ed into *dev_error by kernels. */
 #define DCP_DEVERR_OUT_OF_RANGE 0x1 /* page value / source index outside its pool       */
 #define DCP_DEVERR_TIMEOUT 0x2      /* an mbarrier wait exceeded its limit; unit skipped */
+#define DCP_DEVERR_PLAN_MISMATCH 0x4 /* a planned run found no plan for its arguments in the
+                                        workspace; nothing was computed                      */
 
 #define DCP_PAGE_TOKENS 64
 #define DCP_K_DIM 576
@@ -256,8 +258,10 @@ size_t dcp_partial_decode_attn_workspace_size(int num_requests, int q_len, int n
  *   seq_lens int32 [num_requests], tokens of b including the q_len new ones (>= q_len)
  *   req_page_ptr int64 [num_requests+1], dst_vpages int32 [num_pages]: page table
  *   kv_pools HOST array [n_dcp] of device pointers, each one layer: [slots_per_rank][64][576]
- *            (BF16 or E4M3 per dtype).  Rows at positions >= seq_lens[b] in a request's last
- *            page are masked but must hold finite values.
+ *            (BF16 or E4M3 per dtype).  Rows at positions >= seq_lens[b] (the ragged tail of a
+ *            request's last page) are not part of the sequence and may hold any bytes, NaN
+ *            included: they are masked out of the softmax and cleared in shared memory before
+ *            the P*V product reads them.
  *   o_part   fp32 [n_dcp][num_requests][q_len][num_heads][512]
  *   lse_part fp32 [n_dcp][num_requests][q_len][num_heads]  (natural log)
  *   With only_rank = d >= 0 only rank d's slices of o_part / lse_part are written.
@@ -309,8 +313,12 @@ int dcp_decode_attn_merged(int num_requests, int q_len, int num_heads, const voi
  * number of runs (each run leaves the plan ready for the next).  Runs must use the same
  * num_requests, q_len, num_heads, page table (req_page_ptr, num_pages, dst_vpages), dtype,
  * n_dcp, slots_per_rank and only_rank as the plan, and the same workspace; q, seq_lens (with
- * the same page counts), pools and scales may differ per run.  Nothing checks that the
- * workspace holds a matching plan.  Calls on one workspace must not overlap on the GPU.
+ * the same page counts), pools and scales may differ per run.  The plan stores a key of the
+ * arguments it was made for (sizes, dtype, n_dcp, slots_per_rank, only_rank) and the page
+ * table's last CSR offset; a run whose own differ, or a workspace that holds no plan, sets
+ * DCP_DEVERR_PLAN_MISMATCH in *dev_error and computes nothing (outputs untouched; the
+ * workspace is not written).  Changing the page table's contents at the same sizes is not
+ * detected: make a new plan.  Calls on one workspace must not overlap on the GPU.
  * Returns the statuses of dcp_partial_decode_attn.
  */
 int dcp_attn_plan(int num_requests, int q_len, int num_heads, const int64_t *req_page_ptr,
@@ -344,8 +352,9 @@ int dcp_decode_attn_merged_run(int num_requests, int q_len, int num_heads, const
  * call.
  *   - The first call on a device looks up the array's device address (once per device,
  *     cached); make that first call before any stream capture.
- *   - Sizes whose scratch need (dcp_partial_decode_attn_workspace_size for the same
- *     arguments and dtype) exceeds DCP_STATIC_ATTN_SCRATCH_BYTES return DCP_ERR_WORKSPACE.
+ *   - Sizes whose scratch need for the given dtype exceeds DCP_STATIC_ATTN_SCRATCH_BYTES
+ *     return DCP_ERR_WORKSPACE (dcp_partial_decode_attn_workspace_size for the same sizes is
+ *     an upper bound of that need: it covers both dtypes).
  *   - The array keeps the last call's contents; each call rewrites everything it reads
  *     (the plan kernels reset the work counter to zero), so nothing needs clearing.
  *   - All calls share the one array: calls that may overlap on the GPU (other streams or

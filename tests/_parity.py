@@ -21,14 +21,14 @@ def pool_bytes(case) -> list:
     return [p.cpu().view(torch.uint8).numpy() for p in case.pools]
 
 
-def oracle_attention(case, rank=-1, rows=None, qb=None, pools=None):
+def oracle_attention(case, rank=-1, rows=None, qb=None, pools=None, layout=None):
     qb = q_bits(case) if qb is None else qb
     pools = pool_bytes(case) if pools is None else pools
     return oracle.attention(qb, case.seq_lens.cpu().numpy(), case.req_page_ptr.cpu().numpy(),
                             case.dst_vpages.cpu().numpy(), pools,
                             oracle.BF16 if case.dtype == "bf16" else oracle.E4M3, case.kv_scale,
                             case.softmax_scale, case.n_dcp, rank=rank, rows=rows, q_len=case.T,
-                            num_heads=case.H)
+                            num_heads=case.H, layout=layout or getattr(case, "layout", "page"))
 
 
 def compare(o_gpu, lse_gpu, o_ref, lse_ref, what: str, o_tol=O_TOL, lse_tol=LSE_TOL):

@@ -27,6 +27,17 @@ def test_reference_arm_runs_the_oracle_on_the_host():
     assert line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert line["config"]["workload"].startswith("tiny-")
+    assert {"bytes_per_step", "parallelism", "l2"} <= set(line["config"])
+
+
+def test_reference_arm_loads_only_the_oracle():
+    """The oracle arm's inputs are built without the product library (no import, no workspace)."""
+    code = ("import sys, torch; sys.path.insert(0, %r); import bench; "
+            "wl = bench.Workload('tiny', torch.device('cpu'), oracle_only=True); "
+            "assert wl.ws is None; "
+            "assert 'decode_context_paged_gb300' not in sys.modules, 'product imported'; print('ok')") % ROOT
+    out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0 and "ok" in out.stdout, out.stderr[-2000:]
 
 
 @pytest.mark.gpu

@@ -93,6 +93,19 @@ def test_reshard_bit_exact(cuda_device, dtype, lens, n_layers, n_cp, n_dcp, cont
         assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("ctas", [1, 7, 76, 151, 1000])
+def test_reshard_on_forced_grids_bit_exact(cuda_device, monkeypatch, ctas):
+    """The copy kernel's CTA count forced (DCP_RING_CTAS): one CTA, odd counts, the half grid
+    used for long copies, and more CTAs than chunks; the chunk ranges must still tile the work."""
+    monkeypatch.setenv("DCP_RING_CTAS", str(ctas))
+    case = di.reshard_case([3000, 64, 700, 129, 5000], 8, _counts(8, 4), 8, "e4m3", True, seed=ctas,
+                           device=cuda_device)
+    gpu, ref, err = _reshard_both(case)
+    assert err == 0
+    for a, b in zip(gpu, ref):
+        assert np.array_equal(a, b)
+
+
 def test_reshard_single_paths_compose(cuda_device):
     case = di.reshard_case([2000, 900], 6, _counts(6, 3), 4, "e4m3", True, seed=5, device=cuda_device)
     for r in range(3):

@@ -38,3 +38,52 @@ def test_plan_once_run_per_layer_equals_one_call(cuda_device, name, lens, H, T, 
         assert torch.equal(o_r, o_1) and torch.equal(l_r, l_1)
         for a, b in zip(m_r, m_1):
             assert torch.equal(a, b)
+
+
+MISMATCH = [
+    # what differs between the plan and the run
+    ("fewer-requests", dict(B=2)),
+    ("other-dtype", dict(dtype="e4m3")),
+    ("other-heads", dict(H=32)),
+    ("other-ranks", dict(N=2)),
+    ("no-plan", dict(no_plan=True)),
+]
+
+
+@pytest.mark.parametrize("what,change", MISMATCH, ids=[m[0] for m in MISMATCH])
+def test_planned_run_refuses_a_mismatched_plan(cuda_device, what, change):
+    """A planned run whose arguments do not match the plan in the workspace (or a workspace that
+    holds no plan) sets DEVERR_PLAN_MISMATCH and computes nothing: outputs keep their sentinel."""
+    lens, H, N = [1000, 130, 64 * 9 + 5], 64, 4
+    base = di.attention_case(lens, H=H, T=1, n_dcp=N, dtype="bf16", slots_per_rank=None, seed=4, device=cuda_device)
+    run = di.attention_case(lens[:change.get("B", 3)], H=change.get("H", H), T=1, n_dcp=change.get("N", N),
+                            dtype=change.get("dtype", "bf16"), slots_per_rank=None, seed=5, device=cuda_device)
+    ws = dcp.alloc_workspace(3, 1, H, N, base.dst_vpages.numel(), cuda_device)
+    ws.fill_(0)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    if not change.get("no_plan"):
+        dcp.attn_plan((base.B, 1, H), base.req_page_ptr, base.dst_vpages, base.pools, ws, dev_error=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+    need = dcp.workspace_size(run.B, 1, run.H, run.n_dcp, run.dst_vpages.numel())
+    wsr = ws if need <= ws.numel() else torch.cat([ws, torch.zeros(need - ws.numel(), dtype=torch.uint8,
+                                                                   device=cuda_device)])
+    o = torch.full((run.n_dcp, run.B, 1, run.H, 512), 7.0, device=cuda_device)
+    l = torch.full((run.n_dcp, run.B, 1, run.H), 7.0, device=cuda_device)
+    oo = torch.full((run.B, 1, run.H, 512), 7.0, device=cuda_device)
+    lo = torch.full((run.B, 1, run.H), 7.0, device=cuda_device)
+    dcp.decode_attn_merged(run.q, run.seq_lens, run.req_page_ptr, run.dst_vpages, run.pools, run.softmax_scale,
+                           run.kv_scale, o_part=o, lse_part=l, o_out=oo, lse_out=lo, workspace=wsr, dev_error=err,
+                           planned=True)
+    torch.cuda.synchronize()
+    assert int(err.item()) & dcp.DEVERR_PLAN_MISMATCH
+    assert dcp.device_error_status(int(err.item())) == -4  # DCP_ERR_WORKSPACE
+    for t in (o, l, oo, lo):
+        assert bool((t == 7.0).all())
+    # the matching run afterwards is fine
+    if not change.get("no_plan") and wsr is ws:
+        err.zero_()
+        dcp.decode_attn_merged(base.q, base.seq_lens, base.req_page_ptr, base.dst_vpages, base.pools,
+                               base.softmax_scale, base.kv_scale, workspace=ws, dev_error=err, planned=True)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
