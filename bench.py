@@ -50,12 +50,15 @@ L2_BYTES = 129 << 20  # GB300 L2
 # on (for the reshard: dcp_reshard.cu and the copy ring header); a changed source reports
 # traffic null until it is re-measured.
 NCU_TRAFFIC = {
-    # (kernel, workload): (source hash, DRAM bytes per launch)
-    ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("688cc21d0eb99b1d", 551600768),
-    ("reshard_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("688cc21d0eb99b1d", 5485940480),
-    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("cdc1671979cd698a", 328198912),
-    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("cdc1671979cd698a", 2916891744),
-    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("cdc1671979cd698a", 2587413368),
+    # (kernel, workload): (source hash, DRAM bytes per launch).  Captures on smaller cases of the
+    # same kernel (the agent8 / long1 configs, and agent8's reshard on the long-copy grid) are
+    # scaled by the units processed: pages for the reshard, requests for the attention.
+    ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("26b6b9b40d4d64dd", 552448000),
+    ("reshard_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("26b6b9b40d4d64dd", 5236858368),
+    ("reshard_kernel", "e2e-64x463936-h64-q1-e4m3-dcp8-L8-cp4"): ("26b6b9b40d4d64dd", 44745598653),
+    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("36452c35a093da07", 325319168),
+    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("36452c35a093da07", 2871364608),
+    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("36452c35a093da07", 2550024192),
 }
 
 
@@ -141,6 +144,10 @@ WORKLOADS = {
     "agent": (lambda: [100_000] * 48, 64, 1, 8, "e4m3", 1, 1, 9408),
     "long": (lambda: [1 << 20] * 4, 64, 4, 8, "e4m3", 1, 1, 8192),
     "e2e": (lambda: di.e2e_lengths(), 64, 1, 8, "e4m3", di.E2E_LAYERS, di.E2E_NCP, None),
+    # smaller cases of the same kernels, for profiler captures (not bench lines): 8 of the agent
+    # workload's requests, 1 of the long workload's
+    "agent8": (lambda: [100_000] * 8, 64, 1, 8, "e4m3", 1, 1, 1568),
+    "long1": (lambda: [1 << 20], 64, 4, 8, "e4m3", 1, 1, 2048),
 }
 
 
@@ -485,6 +492,16 @@ def run_ours(args):
     torch.cuda.synchronize()
     if int(wl.err.item()) != 0:
         raise RuntimeError(f"device error word {int(wl.err.item())}")
+    if args.profile_steps:
+        # for a profiler: the warm-up and K plain steps, nothing else (no soak, no timing, no
+        # host-buffer run, no oracle); prints no bench line
+        for _ in range(args.steps):
+            wl.step(dcp)
+        torch.cuda.synchronize()
+        if int(wl.err.item()) != 0:
+            raise RuntimeError(f"device error word {int(wl.err.item())}")
+        print(f"profile run: {wl.name}, {max(args.warmup, 3)} + {args.steps} steps", flush=True)
+        return
 
     # ---- timed region: K steps between two CUDA events on the launching stream.  Then a second
     # timed pass of K steps with events around every stage (stage times, the roofline's kernel
@@ -684,6 +701,8 @@ def main():
     ap.add_argument("--no-plan-overlap", action="store_true",
                     help="make the attention plan inside every attention call instead of once per step on a "
                          "side stream overlapped with the reshard")
+    ap.add_argument("--profile-steps", action="store_true",
+                    help="run only the warm-up and --steps plain steps (for ncu captures; no bench line)")
     ap.add_argument("--unfused", action="store_true",
                     help="partial attention and the LSE merge as separate calls (default: one call)")
     args = ap.parse_args()

@@ -50,8 +50,7 @@ namespace dcp {
 namespace {
 
 constexpr uint32_t kKSlotBytes = 16384;  // K-stream ring slot
-constexpr int kVSlots = 2;               // V-stream ring: 32 KB units
-constexpr uint32_t kVSlotBytes = 32768;
+constexpr int kMaxVSlots = 8;            // V-stream ring slots (upper bound of the configurations)
 constexpr uint32_t kQBytes = 73728;      // 64 rows x 576 BF16, or 128 rows (hi, lo) x 576 E4M3
 constexpr uint32_t kPBytes = 16384;      // one P^T buffer
 constexpr int kGroupRows = 64;
@@ -81,6 +80,21 @@ constexpr float kPScale = 4.f;           // FP8 P is stored as 4 * p (p <= 2^6 u
 #ifndef DCP_ATTN_P_BUFS_F8
 #define DCP_ATTN_P_BUFS_F8 1
 #endif
+// V-stream ring: slots of DCP_ATTN_V_BLOCKS_* blocks, a block being one M-tile of the P*V
+// product for the tile's 128 tokens (BF16: two 64-dim TMA boxes, 32 KB; E4M3: one 128-dim box,
+// 16 KB).
+#ifndef DCP_ATTN_V_SLOTS_BF16
+#define DCP_ATTN_V_SLOTS_BF16 2
+#endif
+#ifndef DCP_ATTN_V_BLOCKS_BF16
+#define DCP_ATTN_V_BLOCKS_BF16 1
+#endif
+#ifndef DCP_ATTN_V_SLOTS_F8
+#define DCP_ATTN_V_SLOTS_F8 2
+#endif
+#ifndef DCP_ATTN_V_BLOCKS_F8
+#define DCP_ATTN_V_BLOCKS_F8 2
+#endif
 
 template <bool F8>
 struct Cfg {
@@ -88,13 +102,16 @@ struct Cfg {
     // slower for both element types).
     static constexpr int kKSlots = F8 ? DCP_ATTN_K_SLOTS_F8 : DCP_ATTN_K_SLOTS_BF16;
     static constexpr int kPBufs = F8 ? DCP_ATTN_P_BUFS_F8 : DCP_ATTN_P_BUFS_BF16;
+    static constexpr int kVSlots = F8 ? DCP_ATTN_V_SLOTS_F8 : DCP_ATTN_V_SLOTS_BF16;
+    static constexpr int kVBlk = F8 ? DCP_ATTN_V_BLOCKS_F8 : DCP_ATTN_V_BLOCKS_BF16;  // M-tiles per V slot
+    static constexpr uint32_t kVSlotBytes = kVBlk * 32768u / (F8 ? 2u : 1u);
+    static constexpr int kVUnits = 4 / kVBlk;       // V-stream units per tile
     static constexpr uint32_t kOffV = kKSlots * kKSlotBytes;
     static constexpr uint32_t kOffQ = kOffV + kVSlots * kVSlotBytes;
     static constexpr uint32_t kOffP = kOffQ + kQBytes;
     static constexpr uint32_t kOffCtl = kOffP + kPBufs * kPBytes;
     static constexpr float kLazyTauV = F8 ? 6.f : 8.f;  // log2 margin of the lazy maximum
     static constexpr int kKBlocks = F8 ? 5 : 9;     // K-stream blocks per tile
-    static constexpr int kVUnits = F8 ? 2 : 4;      // V-stream units per tile
     static constexpr int kSCols = F8 ? 128 : 64;    // TMEM columns per S buffer (hi, lo for FP8)
     static constexpr int kSBufs = F8 ? DCP_ATTN_S_BUFS_F8 : DCP_ATTN_S_BUFS_BF16;
     static constexpr uint32_t kIdescS = F8 ? idesc_e4m3_f32(128, 128, 0, 0) : idesc_bf16_f32(128, 64, 0, 0);
@@ -115,7 +132,7 @@ struct __align__(16) Ctl {
     float oscale[64];
     float qscale[64];            // per query column: softmax_scale * kappa * log2(e) (* 2^-qexp for FP8)
     uint64_t kfull[8], kempty[8];
-    uint64_t vfull[kVSlots], vempty[kVSlots];
+    uint64_t vfull[kMaxVSlots], vempty[kMaxVSlots];
     uint64_t vland;              // V units that need their tail rows cleared land here first
     uint64_t q_full, q_empty;
     uint64_t s_full[3], s_free[3];
@@ -129,6 +146,8 @@ struct __align__(16) Ctl {
 template <bool F8>
 constexpr size_t smem_bytes() { return 1024 + Cfg<F8>::kOffCtl + sizeof(Ctl); }
 static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448, "shared memory budget");
+static_assert(Cfg<false>::kVSlots <= kMaxVSlots && Cfg<true>::kVSlots <= kMaxVSlots, "V ring slots");
+static_assert(4 % Cfg<false>::kVBlk == 0 && 4 % Cfg<true>::kVBlk == 0, "V slot blocks divide the 4 M-tiles");
 
 struct AttnMaps {
     CUtensorMap q[2];                  // BF16: [0] 64x64 boxes.  FP8 (hi|lo rows): [0] 128x64 SW128, [1] 64x64 SW64
@@ -328,7 +347,7 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
             mbar_init(&ctl->kfull[i], 1);
             mbar_init(&ctl->kempty[i], 1);
         }
-        for (int i = 0; i < kVSlots; ++i) {
+        for (int i = 0; i < C::kVSlots; ++i) {
             mbar_init(&ctl->vfull[i], 1);
             mbar_init(&ctl->vempty[i], 1);
         }
@@ -583,21 +602,24 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     }
                     const bool fix = nv0 < 64 || nv1 < 64;
                     for (int vu = 0; vu < C::kVUnits; ++vu) {
-                        const uint32_t slot = vpos % kVSlots;
-                        if (!mbar_wait(&ctl->vempty[slot], ((vpos / kVSlots) & 1) ^ 1, abort_flag, p.dev_error, lim)) {
+                        const uint32_t slot = vpos % C::kVSlots;
+                        if (!mbar_wait(&ctl->vempty[slot], ((vpos / C::kVSlots) & 1) ^ 1, abort_flag, p.dev_error, lim)) {
                             ok = false;
                             break;
                         }
                         ++vpos;
-                        uint8_t *dst = vring + slot * kVSlotBytes;
+                        uint8_t *dst = vring + slot * C::kVSlotBytes;
                         uint64_t *bar = fix ? &ctl->vland : &ctl->vfull[slot];
                         via_land = fix ? (via_land | (1u << slot)) : (via_land & ~(1u << slot));
                         land_pending = fix;
-                        mbar_arrive_expect_tx(bar, kVSlotBytes);
-                        const int w = F8 ? 128 : 64;  // dims per block
+                        mbar_arrive_expect_tx(bar, C::kVSlotBytes);
+                        // the slot holds kBoxCols columns of 128-byte boxes (64 BF16 / 128 E4M3
+                        // dims), each of both pages: [box column][page][64 rows][128 B]
+                        constexpr int kBoxCols = (int)(C::kVSlotBytes / 16384);
+                        const int w = F8 ? 128 : 64;
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int x = (2 * vu + h) * w;
+                        for (int h = 0; h < kBoxCols; ++h) {
+                            const int x = (kBoxCols * vu + h) * w;
                             tma_load_2d_hint(dst + h * 16384, km, bar, x, r0, pol);
                             tma_load_2d_hint(dst + h * 16384 + 8192, km, bar, x, r1, pol);
                         }
@@ -611,7 +633,7 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                             // a row of one 64-dim (BF16) or 128-dim (E4M3) block is 128 contiguous
                             // bytes whatever the swizzle: clear rows [nv, 64) of each page
 #pragma unroll 1
-                            for (int h = 0; h < 2; ++h)
+                            for (int h = 0; h < kBoxCols; ++h)
 #pragma unroll 1
                                 for (int pg = 0; pg < 2; ++pg) {
                                     uint4 *row = reinterpret_cast<uint4 *>(dst + h * 16384 + pg * 8192);
@@ -625,8 +647,9 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
             }
             if (!ok) {  // let issued TMA copies land before the CTA can exit (bounded waits)
                 int never = 0;
-                for (uint32_t q = vpos > (uint32_t)kVSlots ? vpos - kVSlots : 0; q < vpos; ++q)
-                    if (!((via_land >> (q % kVSlots)) & 1u)) mbar_wait(&ctl->vfull[q % kVSlots], (q / kVSlots) & 1, &never, nullptr, lim);
+                for (uint32_t q = vpos > (uint32_t)C::kVSlots ? vpos - C::kVSlots : 0; q < vpos; ++q)
+                    if (!((via_land >> (q % C::kVSlots)) & 1u))
+                        mbar_wait(&ctl->vfull[q % C::kVSlots], (q / C::kVSlots) & 1, &never, nullptr, lim);
                 if (land_pending) mbar_wait(&ctl->vland, land_cnt & 1, &never, nullptr, lim);
             }
         }
@@ -656,34 +679,33 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     }
                     tc_fence_after();
                     for (int vu = 0; vu < C::kVUnits; ++vu) {
-                        const uint32_t slot = vpos % kVSlots;
-                        if (!mbar_wait(&ctl->vfull[slot], (vpos / kVSlots) & 1, abort_flag, p.dev_error, lim)) {
+                        const uint32_t slot = vpos % C::kVSlots;
+                        if (!mbar_wait(&ctl->vfull[slot], (vpos / C::kVSlots) & 1, abort_flag, p.dev_error, lim)) {
                             ok = false;
                             break;
                         }
                         ++vpos;
                         tc_fence_after();
-                        const uint32_t a0 = vaddr + slot * kVSlotBytes;
-                        if (F8) {
+                        const uint32_t a0 = vaddr + slot * C::kVSlotBytes;
 #pragma unroll
-                            for (int h = 0; h < 2; ++h) {  // two 128-dim blocks = two M-tiles
-                                const uint32_t d_tmem = tmem + 64 * (2 * vu + h);
+                        for (int mt = 0; mt < C::kVBlk; ++mt) {  // M-tiles (128 V dims each) of the slot
+                            const uint32_t d_tmem = tmem + 64 * (C::kVBlk * vu + mt);
+                            if (F8) {
 #pragma unroll
                                 for (int kk = 0; kk < 4; ++kk) {
-                                    const uint64_t ad = smem_desc(a0 + h * 16384 + kk * 4096, 16384, 1024, kSwizzle128);
+                                    const uint64_t ad = smem_desc(a0 + mt * 16384 + kk * 4096, 16384, 1024, kSwizzle128);
                                     mma_f8_ss(d_tmem, ad, smem_desc(pb + kk * 2048, 512, 512, kSwizzle64),
                                               C::kIdescPV, !(i == 0 && kk == 0));
                                     mma_f8_ss(d_tmem, ad, smem_desc(pb + 8192 + kk * 2048, 512, 512, kSwizzle64),
                                               C::kIdescPV, 1);
                                 }
-                            }
-                        } else {
-                            const uint32_t d_tmem = tmem + 64 * vu;
+                            } else {
 #pragma unroll
-                            for (int kk = 0; kk < 8; ++kk)
-                                mma_f16_ss(d_tmem, smem_desc(a0 + kk * 2048, 16384, 1024, kSwizzle128),
-                                           smem_desc(pb + kk * 2048, 1024, 1024, kSwizzle128), C::kIdescPV,
-                                           !(i == 0 && kk == 0));
+                                for (int kk = 0; kk < 8; ++kk)
+                                    mma_f16_ss(d_tmem, smem_desc(a0 + mt * 32768 + kk * 2048, 16384, 1024, kSwizzle128),
+                                               smem_desc(pb + kk * 2048, 1024, 1024, kSwizzle128), C::kIdescPV,
+                                               !(i == 0 && kk == 0));
+                            }
                         }
                         mma_commit(&ctl->vempty[slot]);
                     }
@@ -858,14 +880,9 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                         tmem_wait_st();
                     }
                 }
-                // P buffer g % kPBufs: its previous reader must be done.  (Measured: letting
-                // FP8 single-term tiles alternate between the two 8 KB halves of the buffer is
-                // slower; the P*V bursts then delay the score MMAs that free K slots.)
-                if (g >= (uint32_t)C::kPBufs) {
-                    fail = !wait_pv(g - C::kPBufs);
-                    if (fail) continue;
-                    tc_fence_after();
-                }
+                // The weights, packed for the MMA in registers first: only the stores wait for
+                // the P buffer's previous reader (P*V of tile g - kPBufs), which keeps the exp2 and
+                // the conversions off the P*V -> P -> P*V chain.
 #pragma unroll
                 for (int q = 0; q < kCols / 4; ++q) {
                     const float4 m = mr4[q];
@@ -878,33 +895,37 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                         lp[c] += s[c];
                     }
                 }
+                uint4 w0, w1;  // FP8: hi and lo E4M3 terms; BF16: columns 0-7 and 8-15
+                if (F8) {
+                    split_e4m3x4(s[0] * kPScale, s[1] * kPScale, s[2] * kPScale, s[3] * kPScale, w0.x, w1.x);
+                    split_e4m3x4(s[4] * kPScale, s[5] * kPScale, s[6] * kPScale, s[7] * kPScale, w0.y, w1.y);
+                    split_e4m3x4(s[8] * kPScale, s[9] * kPScale, s[10] * kPScale, s[11] * kPScale, w0.z, w1.z);
+                    split_e4m3x4(s[12] * kPScale, s[13] * kPScale, s[14] * kPScale, s[15] * kPScale, w0.w, w1.w);
+                } else {
+                    w0 = make_uint4(pack_bf16(s[0], s[1]), pack_bf16(s[2], s[3]), pack_bf16(s[4], s[5]),
+                                    pack_bf16(s[6], s[7]));
+                    w1 = make_uint4(pack_bf16(s[8], s[9]), pack_bf16(s[10], s[11]), pack_bf16(s[12], s[13]),
+                                    pack_bf16(s[14], s[15]));
+                }
+                if (g >= (uint32_t)C::kPBufs) {
+                    fail = !wait_pv(g - C::kPBufs);
+                    if (fail) continue;
+                    tc_fence_after();
+                }
                 if (F8) {
                     // P^T row as hi and lo E4M3 rows of 64 bytes, MN-major, 64-byte swizzle;
                     // this warpgroup writes 16-byte chunk wg of each.
                     const uint32_t off = (row >> 3) * 512 + (row & 7) * 64;
                     const uint32_t sw = ((wg ^ ((row >> 1) & 3)) << 4);
                     uint8_t *pbuf = sp + (g % C::kPBufs) * kPBytes;
-                    uint4 hv, lv;
-                    split_e4m3x4(s[0] * kPScale, s[1] * kPScale, s[2] * kPScale, s[3] * kPScale, hv.x, lv.x);
-                    split_e4m3x4(s[4] * kPScale, s[5] * kPScale, s[6] * kPScale, s[7] * kPScale, hv.y, lv.y);
-                    split_e4m3x4(s[8] * kPScale, s[9] * kPScale, s[10] * kPScale, s[11] * kPScale, hv.z, lv.z);
-                    split_e4m3x4(s[12] * kPScale, s[13] * kPScale, s[14] * kPScale, s[15] * kPScale, hv.w, lv.w);
-                    *reinterpret_cast<uint4 *>(pbuf + off + sw) = hv;
-                    *reinterpret_cast<uint4 *>(pbuf + 8192 + off + sw) = lv;
+                    *reinterpret_cast<uint4 *>(pbuf + off + sw) = w0;
+                    *reinterpret_cast<uint4 *>(pbuf + 8192 + off + sw) = w1;
                 } else {
                     // P^T row: 64 BF16 values, MN-major with the 128-byte swizzle; this
                     // warpgroup writes 16-byte chunks 2wg and 2wg + 1.
                     uint8_t *prow = sp + (g % C::kPBufs) * kPBytes + (row >> 3) * 1024 + (row & 7) * 128;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint4 w;
-                        w.x = pack_bf16(s[8 * h + 0], s[8 * h + 1]);
-                        w.y = pack_bf16(s[8 * h + 2], s[8 * h + 3]);
-                        w.z = pack_bf16(s[8 * h + 4], s[8 * h + 5]);
-                        w.w = pack_bf16(s[8 * h + 6], s[8 * h + 7]);
-                        const int cc = 2 * wg + h;
-                        *reinterpret_cast<uint4 *>(prow + ((cc ^ (row & 7)) << 4)) = w;
-                    }
+                    *reinterpret_cast<uint4 *>(prow + (((2 * wg) ^ (row & 7)) << 4)) = w0;
+                    *reinterpret_cast<uint4 *>(prow + (((2 * wg + 1) ^ (row & 7)) << 4)) = w1;
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
