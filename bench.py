@@ -148,6 +148,8 @@ WORKLOADS = {
     # workload's requests, 1 of the long workload's
     "agent8": (lambda: [100_000] * 8, 64, 1, 8, "e4m3", 1, 1, 1568),
     "long1": (lambda: [1 << 20], 64, 4, 8, "e4m3", 1, 1, 2048),
+    # a small multi-layer case (CP2 -> DCP4, 4 layers) for the tests of the layer pipeline
+    "layers4": (lambda: [3000, 700, 64 * 40 + 5], 64, 1, 4, "e4m3", 4, 2, None),
 }
 
 
@@ -157,7 +159,8 @@ class Workload:
     on every DCP rank and the LSE merge."""
 
     def __init__(self, name: str, device, seed: int = 1, fused: bool = True, staging_mb: int = 0,
-                 naive: bool = False, layout: str = "page", overlap_plan: bool = True, oracle_only: bool = False):
+                 naive: bool = False, layout: str = "page", overlap_plan: bool = True, oracle_only: bool = False,
+                 overlap_layers: bool = True):
         """oracle_only: inputs for the oracle arm -- the layer split from the oracle, no library
         call, no workspace (that arm loads nothing but the oracle)."""
         if oracle_only:
@@ -180,6 +183,15 @@ class Workload:
         self.lens = lens
         self.B = len(lens)
         counts = [e - s for s, e in (split(self.L, self.n_cp, r) for r in range(self.n_cp))]
+        # layer pipeline (several CP source ranks): the reshard runs per source rank on a stream
+        # of higher priority, and each layer's attention starts as soon as its rank's layers
+        # have arrived, so the attention of the first layers overlaps the transfer of the rest
+        self.layer_rank = [r for r in range(self.n_cp) for _ in range(counts[r])]
+        self.layer_pipe = (overlap_layers and self.overlap_plan and not naive and staging_mb == 0
+                           and layout == "page" and self.n_cp > 1)
+        if self.layer_pipe:
+            self.rs = torch.cuda.Stream(device, priority=-1)
+            self.rank_done = [torch.cuda.Event() for _ in range(self.n_cp)]
         self.rc = di.reshard_case(lens, n_layers=self.L, layer_counts=counts, n_dcp=self.N, dtype=self.dtype,
                                   contiguous_src=True, seed=seed, device=device, dst_slots=slots)
         self.q = di.random_q(self.B, self.T, self.H, di._gen(seed + 7, device), device)
@@ -227,6 +239,8 @@ class Workload:
         # with the plan made once per step: 2 plan launches + per layer (FP8 Q split), attention, 2 merge
         self.launches_per_step = (1 + self.L * 5 if not self.overlap_plan else
                                   3 + self.L * (4 if self.dtype == "e4m3" else 3))
+        if self.layer_pipe:
+            self.launches_per_step += self.n_cp - 1  # one reshard launch per source rank
         if self.naive:
             n_pages = self.rc.dst_vpages.numel()
             need = self.N * self.L * n_pages * self.rc.page_bytes
@@ -261,10 +275,14 @@ class Workload:
                             if fused else dict(self.bytes))
 
     def step(self, dcp, events=None, inputs=None):
-        """events: dict stage -> list of (start, end) event pairs, appended per call.
+        """events: dict stage -> list of (start, end) event pairs, appended per call (the stages
+        then run one after the other, so that each one's time can be attributed).
         inputs: (source pools, q) to use instead of the resident ones."""
         rc = self.rc
         src_pools, q = inputs if inputs is not None else (rc.src_pools, self.q)
+        if self.layer_pipe and events is None:
+            self._pipelined_step(dcp, src_pools, q)
+            return
 
         def rec(stage, fn):
             if events is None:
@@ -328,6 +346,31 @@ class Workload:
             rec("merge", lambda: dcp.lse_merge(self.o_part, self.lse_part, self.o[l], self.lse[l]))
 
 
+
+
+    def _pipelined_step(self, dcp, src_pools, q):
+        rc = self.rc
+        main = torch.cuda.current_stream()
+        self.side.wait_stream(main)  # the previous step's runs are done with the workspace
+        with torch.cuda.stream(self.side):
+            dcp.attn_plan((self.B, self.T, self.H), rc.req_page_ptr, rc.dst_vpages, self.layer_pools[0], self.ws,
+                          dev_error=self.err)
+        self.rs.wait_stream(main)  # the previous step's attention is done with the destination pools
+        with torch.cuda.stream(self.rs):
+            for r in range(self.n_cp):
+                dcp.reshard_pages(rc.req_page_ptr, rc.src_pages, rc.dst_vpages, self.L, src_pools,
+                                  rc.src_pool_pages, rc.dst_pools, rc.dst_slots, only_src_rank=r, dev_error=self.err)
+                self.rank_done[r].record(self.rs)
+        main.wait_stream(self.side)
+        waited = -1
+        for l in range(self.L):
+            if self.layer_rank[l] != waited:
+                waited = self.layer_rank[l]
+                main.wait_event(self.rank_done[waited])
+            dcp.decode_attn_merged(q, self.seq_lens, rc.req_page_ptr, rc.dst_vpages, self.layer_pools[l], self.scale,
+                                   self.kv_scale, o_part=self.o_part, lse_part=self.lse_part, o_out=self.o[l],
+                                   lse_out=self.lse[l], workspace=self.ws, dev_error=self.err, planned=True)
+        main.wait_stream(self.rs)
 
 
 def dist_setup():
@@ -485,7 +528,8 @@ def run_ours(args):
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
     wl = Workload(args.config, dev, seed=1 + rank, fused=not args.unfused, staging_mb=args.staging_mb,
-                  naive=args.naive, layout=args.layout, overlap_plan=not args.no_plan_overlap)
+                  naive=args.naive, layout=args.layout, overlap_plan=not args.no_plan_overlap,
+                  overlap_layers=not args.no_layer_overlap)
 
     for _ in range(max(args.warmup, 3)):
         wl.step(dcp)
@@ -642,6 +686,9 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "e4m3 (fp32 accumulate)",
         "data": "synthetic",
         "config": workload_config(wl, world),
+        "schedule": ("layer pipeline: the reshard per CP source rank on a high-priority stream, each layer's "
+                     "attention as soon as its source rank's layers have arrived (the stage pass below runs "
+                     "the stages one after the other)" if wl.layer_pipe else "stages in order"),
         "stages": {
             "reshard": {"ms": stage_ms["reshard"], "GB/s": stage_gbs["reshard"], "frac_hbm": stage_gbs["reshard"] / hbm,
                         **({"mode": f"bounded pack, {args.staging_mb} MB staging buffer",
@@ -703,6 +750,9 @@ def main():
                          "side stream overlapped with the reshard")
     ap.add_argument("--profile-steps", action="store_true",
                     help="run only the warm-up and --steps plain steps (for ncu captures; no bench line)")
+    ap.add_argument("--no-layer-overlap", action="store_true",
+                    help="several CP source ranks: reshard all layers before the first attention instead of "
+                         "starting each layer's attention as soon as its source rank's layers have arrived")
     ap.add_argument("--unfused", action="store_true",
                     help="partial attention and the LSE merge as separate calls (default: one call)")
     args = ap.parse_args()

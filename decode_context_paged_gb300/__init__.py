@@ -39,6 +39,7 @@ DCP_KV_FP8_E4M3 = 1
 DEVERR_OUT_OF_RANGE = 0x1
 DEVERR_TIMEOUT = 0x2
 DEVERR_PLAN_MISMATCH = 0x4
+DEVERR_LAYOUT = 0x8
 PAGE = 64
 K_DIM = 576
 V_DIM = 512

@@ -62,6 +62,7 @@ int dcp_device_error_status(int32_t word) {
     if (word & DCP_DEVERR_TIMEOUT) return DCP_ERR_TIMEOUT;
     if (word & DCP_DEVERR_OUT_OF_RANGE) return DCP_ERR_OUT_OF_RANGE;
     if (word & DCP_DEVERR_PLAN_MISMATCH) return DCP_ERR_WORKSPACE;
+    if (word & DCP_DEVERR_LAYOUT) return DCP_ERR_UNSUPPORTED;
     return DCP_OK;
 }
 

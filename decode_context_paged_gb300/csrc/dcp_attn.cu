@@ -51,11 +51,13 @@ namespace {
 
 constexpr uint32_t kKSlotBytes = 16384;  // K-stream ring slot
 constexpr int kMaxVSlots = 8;            // V-stream ring slots (upper bound of the configurations)
+constexpr int kMaxKSlots = 8;            // K-stream ring slots (upper bound of the configurations)
 constexpr uint32_t kQBytes = 73728;      // 64 rows x 576 BF16, or 128 rows (hi, lo) x 576 E4M3
 constexpr uint32_t kPBytes = 16384;      // one P^T buffer
 constexpr int kGroupRows = 64;
 constexpr int kThreads = 640;            // 0 K-TMA, 1 S-MMA, 2 V-TMA, 3 PV-MMA, 4-19 softmax
 constexpr int kCols = 16;                // query columns per softmax warpgroup
+constexpr int kSoftmaxWarps = 16;        // arrivals on the barriers the softmax warps release (one per warp)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 256;          // S buffers start at TMEM column 256 (O^T uses 0..255)
 constexpr int kMaxTpc = 4096;
@@ -95,18 +97,30 @@ constexpr float kPScale = 4.f;           // FP8 P is stored as 4 * p (p <= 2^6 u
 #ifndef DCP_ATTN_V_BLOCKS_F8
 #define DCP_ATTN_V_BLOCKS_F8 2
 #endif
+// E4M3: one ring for both products.  A tile's four 128-dim blocks of K rows (16 KB each: 128
+// latent dims x 2 pages) serve the score MMAs as K and stay resident until the P*V MMAs have
+// used them as V, so V is never loaded a second time; the 64-dim rope block has a slot of its
+// own and is freed by the score MMAs.  DCP_ATTN_D_SLOTS_F8 blocks = 2 tiles of lookahead.
+#ifndef DCP_ATTN_UNIFIED_F8
+#define DCP_ATTN_UNIFIED_F8 1
+#endif
+#ifndef DCP_ATTN_D_SLOTS_F8
+#define DCP_ATTN_D_SLOTS_F8 8
+#endif
 
 template <bool F8>
 struct Cfg {
-    // Four K slots and one P buffer (measured: trading a K slot for a second P buffer is
-    // slower for both element types).
-    static constexpr int kKSlots = F8 ? DCP_ATTN_K_SLOTS_F8 : DCP_ATTN_K_SLOTS_BF16;
+    // BF16: four K slots and one P buffer (measured: trading a K slot for a second P buffer is
+    // slower), a V ring of 2 x 32 KB.  E4M3: the unified ring (8 x 16 KB + the rope slot).
+    static constexpr bool kUnified = F8 && DCP_ATTN_UNIFIED_F8;
+    static constexpr int kKSlots = kUnified ? DCP_ATTN_D_SLOTS_F8 : F8 ? DCP_ATTN_K_SLOTS_F8 : DCP_ATTN_K_SLOTS_BF16;
     static constexpr int kPBufs = F8 ? DCP_ATTN_P_BUFS_F8 : DCP_ATTN_P_BUFS_BF16;
-    static constexpr int kVSlots = F8 ? DCP_ATTN_V_SLOTS_F8 : DCP_ATTN_V_SLOTS_BF16;
+    static constexpr int kVSlots = kUnified ? 0 : F8 ? DCP_ATTN_V_SLOTS_F8 : DCP_ATTN_V_SLOTS_BF16;
     static constexpr int kVBlk = F8 ? DCP_ATTN_V_BLOCKS_F8 : DCP_ATTN_V_BLOCKS_BF16;  // M-tiles per V slot
     static constexpr uint32_t kVSlotBytes = kVBlk * 32768u / (F8 ? 2u : 1u);
     static constexpr int kVUnits = 4 / kVBlk;       // V-stream units per tile
-    static constexpr uint32_t kOffV = kKSlots * kKSlotBytes;
+    static constexpr uint32_t kOffRope = kKSlots * kKSlotBytes;             // unified ring: the rope slot
+    static constexpr uint32_t kOffV = kOffRope + (kUnified ? 8192u : 0u);
     static constexpr uint32_t kOffQ = kOffV + kVSlots * kVSlotBytes;
     static constexpr uint32_t kOffP = kOffQ + kQBytes;
     static constexpr uint32_t kOffCtl = kOffP + kPBufs * kPBytes;
@@ -116,6 +130,10 @@ struct Cfg {
     static constexpr int kSBufs = F8 ? DCP_ATTN_S_BUFS_F8 : DCP_ATTN_S_BUFS_BF16;
     static constexpr uint32_t kIdescS = F8 ? idesc_e4m3_f32(128, 128, 0, 0) : idesc_bf16_f32(128, 64, 0, 0);
     static constexpr uint32_t kIdescPV = F8 ? idesc_e4m3_f32(128, 64, 1, 1) : idesc_bf16_f32(128, 64, 1, 1);
+    // The swizzled buffers need 1024-byte alignment.  The dynamic shared memory of a CTA starts
+    // 1024-aligned (after the 1 KB the system reserves); the unified ring's layout uses that and
+    // reserves no alignment slack (the kernel checks the alignment before anything else).
+    static constexpr uint32_t kPad = kUnified ? 0u : 1024u;
 };
 
 struct UnitInfo {
@@ -131,7 +149,8 @@ struct __align__(16) Ctl {
     float corr[64];
     float oscale[64];
     float qscale[64];            // per query column: softmax_scale * kappa * log2(e) (* 2^-qexp for FP8)
-    uint64_t kfull[8], kempty[8];
+    uint64_t kfull[kMaxKSlots], kempty[kMaxKSlots];
+    uint64_t rfull, rempty;      // unified ring: the rope slot
     uint64_t vfull[kMaxVSlots], vempty[kMaxVSlots];
     uint64_t vland;              // V units that need their tail rows cleared land here first
     uint64_t q_full, q_empty;
@@ -144,9 +163,11 @@ struct __align__(16) Ctl {
     int abort_flag;
 };
 template <bool F8>
-constexpr size_t smem_bytes() { return 1024 + Cfg<F8>::kOffCtl + sizeof(Ctl); }
+constexpr size_t smem_bytes() { return Cfg<F8>::kPad + Cfg<F8>::kOffCtl + sizeof(Ctl); }
 static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448, "shared memory budget");
 static_assert(Cfg<false>::kVSlots <= kMaxVSlots && Cfg<true>::kVSlots <= kMaxVSlots, "V ring slots");
+static_assert(Cfg<false>::kKSlots <= kMaxKSlots && Cfg<true>::kKSlots <= kMaxKSlots, "K ring slots");
+static_assert(Cfg<true>::kVUnits > 0 && Cfg<false>::kVUnits > 0, "V units per tile");
 static_assert(4 % Cfg<false>::kVBlk == 0 && 4 % Cfg<true>::kVBlk == 0, "V slot blocks divide the 4 M-tiles");
 
 struct AttnMaps {
@@ -331,6 +352,10 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
     using C = Cfg<F8>;
     constexpr float kLazyTau = C::kLazyTauV;
     extern __shared__ uint8_t smem_raw[];
+    if (C::kPad == 0 && (smem_u32(smem_raw) & 1023u) != 0) {  // (uniform: every CTA returns)
+        if (threadIdx.x == 0 && p.dev_error) atomicOr(p.dev_error, DCP_DEVERR_LAYOUT);
+        return;
+    }
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *kring = base;
     uint8_t *vring = base + C::kOffV;
@@ -352,21 +377,23 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
             mbar_init(&ctl->vempty[i], 1);
         }
         mbar_init(&ctl->vland, 1);
+        mbar_init(&ctl->rfull, 1);
+        mbar_init(&ctl->rempty, 1);
         mbar_init(&ctl->q_full, 1);
         mbar_init(&ctl->q_empty, 1);
         for (int i = 0; i < 3; ++i) {
             mbar_init(&ctl->s_full[i], 1);
-            mbar_init(&ctl->s_free[i], 512);
+            mbar_init(&ctl->s_free[i], kSoftmaxWarps);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&ctl->unit_full[i], 1);
             mbar_init(&ctl->unit_empty[i], 7);
         }
-        mbar_init(&ctl->p_full[0], 512);
-        mbar_init(&ctl->p_full[1], 512);
+        mbar_init(&ctl->p_full[0], kSoftmaxWarps);
+        mbar_init(&ctl->p_full[1], kSoftmaxWarps);
         mbar_init(&ctl->o_done[0], 1);
         mbar_init(&ctl->o_done[1], 1);
-        mbar_init(&ctl->o_free, 512);
+        mbar_init(&ctl->o_free, kSoftmaxWarps);
         mbar_init(&ctl->drain_s, 1);
         mbar_init(&ctl->drain_pv, 1);
         ctl->abort_flag = 0;
@@ -409,14 +436,41 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
         ja = p.comp_page[u.comp_base + pg];
         jb = (pg + 1 < u.n_pages) ? p.comp_page[u.comp_base + pg + 1] : -1;
     };
+    // Rows of the page with index j (within the request) that hold positions < seq.  Rows past
+    // the request's length are not part of the sequence and may hold any bytes (NaN included):
+    // P is zero there, but 0 x NaN would reach O, so the stream that feeds P*V clears them in
+    // shared memory before releasing the block (it lands on vland first).
+    auto valid_rows = [&](int j, int seq) -> int {
+        long long nv;
+        if (p.tok_n == 0) {
+            nv = (long long)seq - 64LL * j;
+        } else {
+            const int c = j % p.tok_n;
+            nv = seq > c ? ((long long)seq - c + p.tok_n - 1) / p.tok_n - 64LL * (j / p.tok_n) : 0;
+        }
+        return (int)(nv < 0 ? 0 : nv > 64 ? 64 : nv);
+    };
+    // Clear rows [nv, 64) of both pages of one 16 KB block ([page][64 rows][128 B]; a 128-byte row
+    // of a block is contiguous whatever the swizzle).
+    auto clear_tail = [&](uint8_t *blk, int nv0, int nv1) {
+#pragma unroll 1
+        for (int pg = 0; pg < 2; ++pg) {
+            uint4 *row = reinterpret_cast<uint4 *>(blk + pg * 8192);
+            for (int e = (pg ? nv1 : nv0) * 8; e < 64 * 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
+        }
+    };
 
     if (warp == 0) {
         // ---------------------------------------------------------------- K-stream TMA
         if (lane == 0) {
             prefetch_tmap(&maps.q[0]);
-            const uint64_t pol = make_policy_evict_last();
-            uint32_t kpos = 0, q_cnt = 0, k = 0;
-            bool ok = true;
+            // K rows are read again: from L2 by the V stream (separate V ring), or by the other
+            // query groups of the same chunk (q_len > 1 or more than 64 heads).  Otherwise (the
+            // unified ring, one query group) each row is read once.
+            const uint64_t pol = (C::kUnified && p.G == 1) ? make_policy_evict_first() : make_policy_evict_last();
+            uint32_t kpos = 0, q_cnt = 0, k = 0, rpos = 0, land_cnt = 0;
+            uint32_t via_land = 0;  // unified ring: bit per slot, its latest block went through vland
+            bool ok = true, land_pending = false;
             while (ok) {
                 const int e = k & 1;
                 if (!mbar_wait(&ctl->unit_empty[e], ((k >> 1) & 1) ^ 1, abort_flag, p.dev_error, lim)) {
@@ -464,12 +518,35 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                         tma_load_2d(sq + kb * 8192, &maps.q[0], &ctl->q_full, kb * 64, u.q_row0);
                 }
                 const CUtensorMap *km = maps.kv[u.d];
-                int rn0, rn1;
+                int rn0, rn1, jn0 = 0, jn1 = -1;
+                const int seq = p.seq_lens[u.b];
                 tile_rows(u, 0, rn0, rn1);
+                if (C::kUnified) tile_pages(u, 0, jn0, jn1);
                 for (int i = 0; i < nt && ok; ++i) {
                     const int r0 = rn0, r1 = rn1;
-                    if (i + 1 < nt) tile_rows(u, i + 1, rn0, rn1);
+                    int nv0 = 64, nv1 = 64;
+                    if (C::kUnified) {
+                        nv0 = valid_rows(jn0, seq);
+                        nv1 = jn1 >= 0 ? valid_rows(jn1, seq) : 64;  // a missing page is zero-filled
+                    }
+                    if (i + 1 < nt) {  // the next tile's page metadata, a tile ahead
+                        tile_rows(u, i + 1, rn0, rn1);
+                        if (C::kUnified) tile_pages(u, i + 1, jn0, jn1);
+                    }
+                    const bool fix = nv0 < 64 || nv1 < 64;
                     for (int kb = 0; kb < C::kKBlocks; ++kb) {
+                        if (C::kUnified && kb == 4) {  // rope: 64 dims, 64-byte swizzle, 4 KB per page
+                            if (!mbar_wait(&ctl->rempty, (rpos & 1) ^ 1, abort_flag, p.dev_error, lim)) {
+                                ok = false;
+                                break;
+                            }
+                            ++rpos;
+                            uint8_t *dst = kring + C::kOffRope;
+                            mbar_arrive_expect_tx(&ctl->rfull, 8192);
+                            tma_load_2d_hint(dst, &km[1], &ctl->rfull, 512, r0, pol);
+                            tma_load_2d_hint(dst + 4096, &km[1], &ctl->rfull, 512, r1, pol);
+                            continue;
+                        }
                         const uint32_t slot = kpos % kKSlots;
                         if (!mbar_wait(&ctl->kempty[slot], ((kpos / kKSlots) & 1) ^ 1, abort_flag, p.dev_error, lim)) {
                             ok = false;
@@ -483,9 +560,27 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                             tma_load_2d_hint(dst + 4096, &km[1], &ctl->kfull[slot], 512, r1, pol);
                         } else {
                             const int x = F8 ? kb * 128 : kb * 64;
-                            mbar_arrive_expect_tx(&ctl->kfull[slot], kKSlotBytes);
-                            tma_load_2d_hint(dst, &km[0], &ctl->kfull[slot], x, r0, pol);
-                            tma_load_2d_hint(dst + 8192, &km[0], &ctl->kfull[slot], x, r1, pol);
+                            // unified ring: a block with rows past the sequence serves P*V too
+                            const bool via = C::kUnified && fix;
+                            uint64_t *bar = via ? &ctl->vland : &ctl->kfull[slot];
+                            if (C::kUnified) {
+                                via_land = via ? (via_land | (1u << slot)) : (via_land & ~(1u << slot));
+                                land_pending = via;
+                            }
+                            mbar_arrive_expect_tx(bar, kKSlotBytes);
+                            tma_load_2d_hint(dst, &km[0], bar, x, r0, pol);
+                            tma_load_2d_hint(dst + 8192, &km[0], bar, x, r1, pol);
+                            if (via) {
+                                if (!mbar_wait(&ctl->vland, land_cnt & 1, abort_flag, p.dev_error, lim)) {
+                                    ok = false;
+                                    break;
+                                }
+                                ++land_cnt;
+                                land_pending = false;
+                                clear_tail(dst, nv0, nv1);
+                                fence_proxy_async_smem();
+                                mbar_arrive(&ctl->kfull[slot]);
+                            }
                         }
                     }
                 }
@@ -493,14 +588,17 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
             if (!ok) {  // let issued TMA copies land before the CTA can exit (bounded waits)
                 int never = 0;
                 for (uint32_t q = kpos > (uint32_t)kKSlots ? kpos - kKSlots : 0; q < kpos; ++q)
-                    mbar_wait(&ctl->kfull[q % kKSlots], (q / kKSlots) & 1, &never, nullptr, lim);
+                    if (!((via_land >> (q % kKSlots)) & 1u))
+                        mbar_wait(&ctl->kfull[q % kKSlots], (q / kKSlots) & 1, &never, nullptr, lim);
+                if (land_pending) mbar_wait(&ctl->vland, land_cnt & 1, &never, nullptr, lim);
+                if (rpos > 0) mbar_wait(&ctl->rfull, (rpos - 1) & 1, &never, nullptr, lim);
                 if (q_cnt > 0) mbar_wait(&ctl->q_full, (q_cnt - 1) & 1, &never, nullptr, lim);
             }
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- score MMAs
         if (lane == 0) {
-            uint32_t kpos = 0, s_cnt = 0, q_cnt = 0, k = 0;
+            uint32_t kpos = 0, s_cnt = 0, q_cnt = 0, k = 0, rpos = 0;
             bool ok = true;
             const uint32_t kaddr = smem_u32(kring), q_addr = smem_u32(sq);
             UnitInfo u;
@@ -520,14 +618,17 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     tc_fence_after();
                     const uint32_t d_tmem = tmem + kSCol + C::kSCols * sb;
                     for (int kb = 0; kb < C::kKBlocks; ++kb) {
+                        const bool rope_slot = C::kUnified && kb == 4;
                         const uint32_t slot = kpos % kKSlots;
-                        if (!mbar_wait(&ctl->kfull[slot], (kpos / kKSlots) & 1, abort_flag, p.dev_error, lim)) {
+                        if (rope_slot ? !mbar_wait(&ctl->rfull, rpos & 1, abort_flag, p.dev_error, lim)
+                                      : !mbar_wait(&ctl->kfull[slot], (kpos / kKSlots) & 1, abort_flag, p.dev_error, lim)) {
                             ok = false;
                             break;
                         }
-                        ++kpos;
+                        if (rope_slot) ++rpos;
+                        else ++kpos;
                         tc_fence_after();
-                        const uint32_t a0 = kaddr + slot * kKSlotBytes;
+                        const uint32_t a0 = rope_slot ? kaddr + C::kOffRope : kaddr + slot * kKSlotBytes;
                         if (F8) {
                             if (kb < 4) {
                                 const uint32_t b0 = q_addr + kb * 16384;
@@ -551,7 +652,9 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                                            smem_desc(b0 + kk * 32, 16, 1024, kSwizzle128), C::kIdescS,
                                            (kb | kk) != 0);
                         }
-                        mma_commit(&ctl->kempty[slot]);
+                        // unified ring: the latent blocks stay until P*V has read them
+                        if (rope_slot) mma_commit(&ctl->rempty);
+                        else if (!C::kUnified) mma_commit(&ctl->kempty[slot]);
                     }
                     if (!ok) break;
                     mma_commit(&ctl->s_full[sb]);
@@ -564,26 +667,20 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
         }
     } else if (warp == 2) {
         // ---------------------------------------------------------------- V-stream TMA
-        // Rows of a page past the request's length hold no key and may hold any bytes (NaN
-        // included): P is zero there, but 0 x NaN would reach O, so a V unit with such rows
-        // lands on vland first, the rows are cleared, and only then is vfull released.
-        if (lane == 0) {
+        // (unified ring: no V stream; the warp only follows the unit ring)
+        if constexpr (C::kUnified) {
+            if (lane == 0) {
+                uint32_t k = 0;
+                UnitInfo u;
+                while (next_unit(k, u)) {
+                }
+            }
+        } else if (lane == 0) {
             const uint64_t pol = make_policy_evict_first();
             uint32_t vpos = 0, k = 0, land_cnt = 0;
             bool ok = true, land_pending = false;
             uint32_t via_land = 0;  // bit per slot: its latest unit went through vland
             UnitInfo u;
-            // rows of the page with index j (within the request) that hold positions < seq
-            auto valid_rows = [&](int j, int seq) -> int {
-                long long nv;
-                if (p.tok_n == 0) {
-                    nv = (long long)seq - 64LL * j;
-                } else {
-                    const int c = j % p.tok_n;
-                    nv = seq > c ? ((long long)seq - c + p.tok_n - 1) / p.tok_n - 64LL * (j / p.tok_n) : 0;
-                }
-                return (int)(nv < 0 ? 0 : nv > 64 ? 64 : nv);
-            };
             while (ok && next_unit(k, u)) {
                 const int nt = (u.n_pages + 1) >> 1;
                 const CUtensorMap *km = &maps.kv[u.d][0];
@@ -630,15 +727,8 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                             }
                             ++land_cnt;
                             land_pending = false;
-                            // a row of one 64-dim (BF16) or 128-dim (E4M3) block is 128 contiguous
-                            // bytes whatever the swizzle: clear rows [nv, 64) of each page
 #pragma unroll 1
-                            for (int h = 0; h < kBoxCols; ++h)
-#pragma unroll 1
-                                for (int pg = 0; pg < 2; ++pg) {
-                                    uint4 *row = reinterpret_cast<uint4 *>(dst + h * 16384 + pg * 8192);
-                                    for (int e = (pg ? nv1 : nv0) * 8; e < 64 * 8; ++e) row[e] = make_uint4(0, 0, 0, 0);
-                                }
+                            for (int h = 0; h < kBoxCols; ++h) clear_tail(dst + h * 16384, nv0, nv1);
                             fence_proxy_async_smem();
                             mbar_arrive(&ctl->vfull[slot]);
                         }
@@ -658,7 +748,7 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
         if (lane == 0) {
             uint32_t vpos = 0, p_cnt = 0, of_cnt = 0, k = 0;
             bool had_tiles = false, ok = true;
-            const uint32_t vaddr = smem_u32(vring), p_addr = smem_u32(sp);
+            const uint32_t vaddr = smem_u32(vring), p_addr = smem_u32(sp), kaddr = smem_u32(kring);
             UnitInfo u;
             while (ok && next_unit(k, u)) {
                 const int nt = (u.n_pages + 1) >> 1;
@@ -678,36 +768,60 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                         ++of_cnt;
                     }
                     tc_fence_after();
-                    for (int vu = 0; vu < C::kVUnits; ++vu) {
-                        const uint32_t slot = vpos % C::kVSlots;
-                        if (!mbar_wait(&ctl->vfull[slot], (vpos / C::kVSlots) & 1, abort_flag, p.dev_error, lim)) {
-                            ok = false;
-                            break;
-                        }
-                        ++vpos;
-                        tc_fence_after();
-                        const uint32_t a0 = vaddr + slot * C::kVSlotBytes;
-#pragma unroll
-                        for (int mt = 0; mt < C::kVBlk; ++mt) {  // M-tiles (128 V dims each) of the slot
-                            const uint32_t d_tmem = tmem + 64 * (C::kVBlk * vu + mt);
-                            if (F8) {
-#pragma unroll
-                                for (int kk = 0; kk < 4; ++kk) {
-                                    const uint64_t ad = smem_desc(a0 + mt * 16384 + kk * 4096, 16384, 1024, kSwizzle128);
-                                    mma_f8_ss(d_tmem, ad, smem_desc(pb + kk * 2048, 512, 512, kSwizzle64),
-                                              C::kIdescPV, !(i == 0 && kk == 0));
-                                    mma_f8_ss(d_tmem, ad, smem_desc(pb + 8192 + kk * 2048, 512, 512, kSwizzle64),
-                                              C::kIdescPV, 1);
-                                }
-                            } else {
-#pragma unroll
-                                for (int kk = 0; kk < 8; ++kk)
-                                    mma_f16_ss(d_tmem, smem_desc(a0 + mt * 32768 + kk * 2048, 16384, 1024, kSwizzle128),
-                                               smem_desc(pb + kk * 2048, 1024, 1024, kSwizzle128), C::kIdescPV,
-                                               !(i == 0 && kk == 0));
+                    if constexpr (C::kUnified) {
+                        // the tile's four latent blocks, still in the ring since its score MMAs
+                        for (int m = 0; m < 4; ++m) {
+                            const uint32_t slot = vpos % kKSlots;
+                            if (!mbar_wait(&ctl->kfull[slot], (vpos / kKSlots) & 1, abort_flag, p.dev_error, lim)) {
+                                ok = false;
+                                break;
                             }
+                            ++vpos;
+                            tc_fence_after();
+                            const uint32_t a0 = kaddr + slot * kKSlotBytes;
+                            const uint32_t d_tmem = tmem + 64 * m;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {
+                                const uint64_t ad = smem_desc(a0 + kk * 4096, 16384, 1024, kSwizzle128);
+                                mma_f8_ss(d_tmem, ad, smem_desc(pb + kk * 2048, 512, 512, kSwizzle64), C::kIdescPV,
+                                          !(i == 0 && kk == 0));
+                                mma_f8_ss(d_tmem, ad, smem_desc(pb + 8192 + kk * 2048, 512, 512, kSwizzle64),
+                                          C::kIdescPV, 1);
+                            }
+                            mma_commit(&ctl->kempty[slot]);
                         }
-                        mma_commit(&ctl->vempty[slot]);
+                    } else {
+                        for (int vu = 0; vu < C::kVUnits; ++vu) {
+                            const uint32_t slot = vpos % C::kVSlots;
+                            if (!mbar_wait(&ctl->vfull[slot], (vpos / C::kVSlots) & 1, abort_flag, p.dev_error, lim)) {
+                                ok = false;
+                                break;
+                            }
+                            ++vpos;
+                            tc_fence_after();
+                            const uint32_t a0 = vaddr + slot * C::kVSlotBytes;
+#pragma unroll
+                            for (int mt = 0; mt < C::kVBlk; ++mt) {  // M-tiles (128 V dims each) of the slot
+                                const uint32_t d_tmem = tmem + 64 * (C::kVBlk * vu + mt);
+                                if (F8) {
+#pragma unroll
+                                    for (int kk = 0; kk < 4; ++kk) {
+                                        const uint64_t ad = smem_desc(a0 + mt * 16384 + kk * 4096, 16384, 1024, kSwizzle128);
+                                        mma_f8_ss(d_tmem, ad, smem_desc(pb + kk * 2048, 512, 512, kSwizzle64),
+                                                  C::kIdescPV, !(i == 0 && kk == 0));
+                                        mma_f8_ss(d_tmem, ad, smem_desc(pb + 8192 + kk * 2048, 512, 512, kSwizzle64),
+                                                  C::kIdescPV, 1);
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int kk = 0; kk < 8; ++kk)
+                                        mma_f16_ss(d_tmem, smem_desc(a0 + mt * 32768 + kk * 2048, 16384, 1024, kSwizzle128),
+                                                   smem_desc(pb + kk * 2048, 1024, 1024, kSwizzle128), C::kIdescPV,
+                                                   !(i == 0 && kk == 0));
+                                }
+                            }
+                            mma_commit(&ctl->vempty[slot]);
+                        }
                     }
                     if (!ok) break;
                     mma_commit(&ctl->o_done[tile_g & 1]);
@@ -818,7 +932,8 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                         tmem_wait_ld();
                     }
                     tc_fence_before();
-                    mbar_arrive(&ctl->s_free[sb]);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ctl->s_free[sb]);  // one arrival per warp
                     // mask: ragged last page / missing second page / causal limit
                     // position of this row: 64 j + r (page layout), or (64 (j div N) + r) N + j mod N
                     // (token layout: entry j = jj N + d is rank d's local page jj)
@@ -927,9 +1042,10 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     *reinterpret_cast<uint4 *>(prow + (((2 * wg) ^ (row & 7)) << 4)) = w0;
                     *reinterpret_cast<uint4 *>(prow + (((2 * wg + 1) ^ (row & 7)) << 4)) = w1;
                 }
-                fence_proxy_async_smem();
+                fence_proxy_async_smem();  // every writer's P stores, for the MMA's async proxy
                 tc_fence_before();
-                mbar_arrive(&ctl->p_full[g & 1]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctl->p_full[g & 1]);
             }
             if (aborted) break;
             fail = !wait_pv(s_cnt - 1);
@@ -953,19 +1069,26 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
             float osc[kCols];
 #pragma unroll
             for (int c = 0; c < kCols; ++c) osc[c] = ctl->oscale[c0 + c];
-#pragma unroll 1
+            // O^T from TMEM, one 128-dim block at a time; the next block's load is in flight
+            // while this block's stores issue
+            float oa[kCols], ob[kCols];
+            tmem_ld16(tmem + lane_base + c0, oa);
+            tmem_wait_ld();
+#pragma unroll
             for (int j = 0; j < 4; ++j) {
-                float o[kCols];
-                tmem_ld16(tmem + lane_base + 64 * j + c0, o);
-                tmem_wait_ld();
+                float(&cur)[kCols] = (j & 1) ? ob : oa;
+                float(&nxt)[kCols] = (j & 1) ? oa : ob;
+                if (j + 1 < 4) tmem_ld16(tmem + lane_base + 64 * (j + 1) + c0, nxt);
                 const int vcol = j * 128 + row;  // V dimension held by this lane
 #pragma unroll
                 for (int c = 0; c < kCols; ++c)
                     if (c0 + c < u.rows_valid)
-                        obase[(out_row0 + c0 + c) * kVDim + vcol] = o[c] * osc[c];
+                        obase[(out_row0 + c0 + c) * kVDim + vcol] = cur[c] * osc[c];
+                if (j + 1 < 4) tmem_wait_ld();
             }
             tc_fence_before();
-            mbar_arrive(&ctl->o_free);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctl->o_free);
         }
     }
 

@@ -73,6 +73,9 @@ typedef enum { DCP_KV_BF16 = 0, DCP_KV_FP8_E4M3 = 1 } dcp_kv_dtype;
 #define DCP_DEVERR_TIMEOUT 0x2      /* an mbarrier wait exceeded its limit; unit skipped */
 #define DCP_DEVERR_PLAN_MISMATCH 0x4 /* a planned run found no plan for its arguments in the
                                         workspace; nothing was computed                      */
+#define DCP_DEVERR_LAYOUT 0x8       /* the attention kernel's shared-memory layout could not be
+                                       placed (an unaligned dynamic shared-memory base); nothing
+                                       was computed                                          */
 
 #define DCP_PAGE_TOKENS 64
 #define DCP_K_DIM 576

@@ -105,3 +105,29 @@ def test_reference_arm_under_torchrun_prints_once():
     assert len(lines) == 1
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2
+
+
+@pytest.mark.gpu
+def test_layer_pipeline_equals_the_stages_in_order(cuda_device):
+    """The bench's layer pipeline (reshard per source rank on its own stream, each layer's
+    attention after its rank's layers) computes bit for bit what the stages in order compute."""
+    import torch
+    sys.path.insert(0, ROOT)
+    import bench
+    import dcp_inputs as di
+    import decode_context_paged_gb300 as dcp
+    wl = bench.Workload("layers4", cuda_device)
+    assert wl.layer_pipe and wl.L == 4 and wl.n_cp == 2
+    outs = []
+    for pipelined in (True, False, True):
+        for p in wl.rc.dst_pools:
+            p.view(torch.uint8).fill_(di.SENTINEL_BYTE)
+        wl.o.fill_(7.0)
+        wl.lse.fill_(7.0)
+        wl.step(dcp, events=None if pipelined else {})
+        torch.cuda.synchronize()
+        assert int(wl.err.item()) == 0
+        outs.append((wl.o.clone(), wl.lse.clone()))
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(l, outs[0][1])
+    assert bool(torch.isfinite(outs[0][0]).all())
