@@ -112,18 +112,28 @@ def consensus_prefix_len(local_len: int, group=None) -> int:
     return int(t.item())
 
 
-_PAD = {dist.ReduceOp.SUM: 0, dist.ReduceOp.MAX: float("-inf"), dist.ReduceOp.MIN: float("inf")}
+def _pad_value(op, dtype: torch.dtype):
+    """The identity of `op` in `dtype` (integers: 0, or the type's extreme for MAX / MIN)."""
+    if op == dist.ReduceOp.SUM:
+        return 0
+    info = torch.finfo(dtype) if dtype.is_floating_point else torch.iinfo(dtype)
+    if op == dist.ReduceOp.MAX:
+        return float("-inf") if dtype.is_floating_point else info.min
+    if op == dist.ReduceOp.MIN:
+        return float("inf") if dtype.is_floating_point else info.max
+    raise ValueError(f"padded_all_reduce: unsupported op {op}")
 
 
 def padded_all_reduce(values: torch.Tensor, op=dist.ReduceOp.SUM, group=None) -> torch.Tensor:
     """All-reduce of 1-D tensors whose length differs per rank: the ranks agree on the longest
     length (an all-reduce MAX every rank joins), pad with op's identity and reduce; every rank
-    joins both collectives whatever its own length (even 0)."""
+    joins both collectives whatever its own length (even 0).  The reduction runs in the values'
+    own dtype, so integers stay exact (every rank must pass the same dtype)."""
     n = torch.tensor([values.numel()], dtype=torch.int64)
     dist.all_reduce(n, op=dist.ReduceOp.MAX, group=group)
     width = int(n.item())
-    buf = torch.full((width,), _PAD[op], dtype=values.dtype if values.dtype.is_floating_point else torch.float64)
-    buf[:values.numel()] = values.to(buf.dtype)
+    buf = torch.full((width,), _pad_value(op, values.dtype), dtype=values.dtype)
+    buf[:values.numel()] = values
     dist.all_reduce(buf, op=op, group=group)
     return buf
 

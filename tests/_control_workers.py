@@ -72,7 +72,12 @@ def _consensus_and_padded(rank, world, dist):
     vals = torch.arange({0: 3, 1: 5, 2: 0}[rank], dtype=torch.float64) + 10 * rank
     s = control.padded_all_reduce(vals, op=dist.ReduceOp.SUM)
     m = control.padded_all_reduce(vals, op=dist.ReduceOp.MAX)
-    return {"prefix": n, "sum": s.tolist(), "max": m.tolist()}
+    # integers past 2^53 stay exact (a float64 reduction would round them)
+    big = torch.tensor([(1 << 60) + 1 + rank] * (rank + 1), dtype=torch.int64)
+    bs = control.padded_all_reduce(big, op=dist.ReduceOp.SUM)
+    bm = control.padded_all_reduce(big, op=dist.ReduceOp.MIN)
+    return {"prefix": n, "sum": s.tolist(), "max": m.tolist(), "big_sum": bs.tolist(), "big_min": bm.tolist(),
+            "big_dtype": str(bs.dtype)}
 
 
 def _gather_and_merge(rank, world, dist):

@@ -91,6 +91,11 @@ def test_consensus_prefix_and_padded_all_reduce():
         assert res["prefix"] == 5
         assert res["sum"] == [0 + 10 + 0, 1 + 11, 2 + 12, 13, 14]
         assert res["max"] == [10, 11, 12, 13, 14]
+        # ranks pass 1, 2, 3 copies of 2^60 + 1 + rank: exact int64 sums and minima
+        b = (1 << 60) + 1
+        assert res["big_dtype"] == "torch.int64"
+        assert res["big_sum"] == [3 * b + 3, 2 * b + 3, b + 2]
+        assert res["big_min"] == [b, b + 1, b + 2]
 
 
 @pytest.mark.parametrize("world", [2, 4])
