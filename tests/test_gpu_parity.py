@@ -222,9 +222,10 @@ def _sampled(case, o, l, om, lm, n_rows, ranks, seed=0):
 
 
 def test_attention_agent_full_size_sampled(cuda_device):
-    """48 x 100,000 tokens, 64 heads, FP8-E4M3, DCP=8 over a ~2.8 GB pool; sampled rows."""
+    """48 x 100,000 tokens, 64 heads, FP8-E4M3, DCP=8 over a ~2.8 GB pool; 64 sampled rows on
+    every rank's partials and the merged output."""
     case = di.agent_case(cuda_device)
-    _sampled(case, *_run_attention(case), n_rows=24, ranks=(0, 7))
+    _sampled(case, *_run_attention(case), n_rows=64, ranks=range(8))
 
 
 def test_attention_agent_dcp1_check(cuda_device):
@@ -244,12 +245,25 @@ def test_attention_agent_dcp1_check(cuda_device):
     o1, l1, _, _ = _run_attention(single)
     compare(om.reshape(-1, 512), lm.reshape(-1), o1[0].reshape(-1, 512).astype(np.float64),
             l1[0].reshape(-1).astype(np.float64), "DCP=1 vs DCP=8 merged")
+    # and the DCP=1 run itself against the oracle (unsharded attention over the one pool)
+    rows = np.sort(np.random.default_rng(1).choice(single.rows, 48, replace=False))
+    ro, rl = oracle_attention(single, rows=rows)
+    compare(o1[0].reshape(-1, 512)[rows], l1[0].reshape(-1)[rows], ro, rl, "agent 6 requests at DCP=1")
 
 
 def test_attention_long_eagle_full_size_sampled(cuda_device):
-    """4 x 1,048,576 tokens, q_len 4 causal, FP8, DCP=8; sampled rows incl. every new token."""
+    """4 x 1,048,576 tokens, q_len 4 causal, FP8, DCP=8: for every request and every one of the
+    4 new tokens, 4 heads, on every rank's partials and the merged output."""
     case = di.long_eagle_case(cuda_device)
-    _sampled(case, *_run_attention(case), n_rows=12, ranks=(3,))
+    o, l, om, lm = _run_attention(case)
+    rows = np.array([(b * case.T + t) * case.H + h for b in range(case.B) for t in range(case.T)
+                     for h in (0, 21, 42, 63)], np.int64)
+    qb, pools = q_bits(case), pool_bytes(case)
+    for d in range(case.n_dcp):
+        ro, rl = oracle_attention(case, rank=d, rows=rows, qb=qb, pools=pools)
+        compare(o[d].reshape(-1, 512)[rows], l[d].reshape(-1)[rows], ro, rl, f"long rank {d}")
+    ro, rl = oracle_attention(case, rows=rows, qb=qb, pools=pools)
+    compare(om.reshape(-1, 512)[rows], lm.reshape(-1)[rows], ro, rl, "long merged")
 
 
 def test_attention_and_merge_with_no_requests(cuda_device):
