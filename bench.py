@@ -56,9 +56,9 @@ NCU_TRAFFIC = {
     ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("26b6b9b40d4d64dd", 552448000),
     ("reshard_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("26b6b9b40d4d64dd", 5236858368),
     ("reshard_kernel", "e2e-64x463936-h64-q1-e4m3-dcp8-L8-cp4"): ("26b6b9b40d4d64dd", 44745598653),
-    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("11acd48542aedf41", 325443072),
-    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("11acd48542aedf41", 2799823872),
-    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("11acd48542aedf41", 2531567616),
+    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("12f2a36df02d7ace", 325443072),
+    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("12f2a36df02d7ace", 2799823872),
+    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("12f2a36df02d7ace", 2531567616),
 }
 
 

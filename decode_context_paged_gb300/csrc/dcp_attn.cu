@@ -19,11 +19,15 @@
 //    page bytes: Q enters as two E4M3 terms (hi + lo, stacked as N = 128 rows, with a
 //    power-of-two scale per query row) so the scores keep BF16-level accuracy, and P enters
 //    as hi + lo terms accumulated into the same O^T.
-//  * Two TMA streams: the K stream (all 576 dims of a tile, read from HBM with an L2
+//  * BF16: two TMA streams.  The K stream (all 576 dims of a tile, read from HBM with an L2
 //    evict-last hint) feeds the score MMAs through a 4-slot ring; the V stream re-reads the
-//    512 latent dims of the same pages (an L2 hit) into a 2-unit ring for P*V.  Separate
-//    MMA-issuing threads for the two products keep HBM loads in flight while the softmax
-//    of an earlier tile runs.
+//    512 latent dims of the same pages (an L2 hit) into a 2-unit ring for P*V.
+//    E4M3: one stream into a unified ring.  The four 128-dim latent blocks of a tile stay in
+//    their slots from the score MMAs to the P*V MMAs, which read them as V; the ring holds two
+//    tiles, plus a slot for the rope block.  Separate MMA-issuing threads for the two products
+//    keep HBM loads in flight while the softmax of an earlier tile runs.
+//  * Rows of a request's last page past its length may hold any bytes: the stream that feeds
+//    P*V clears them in shared memory before the MMA reads them.
 //  * Sixteen softmax warps (four warpgroups of 16 query columns each) own one token row per
 //    thread (TMEM lane = row): scores are masked
 //    (ragged last page, causal limit among the new tokens), column maxima are reduced with a

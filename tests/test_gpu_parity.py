@@ -164,7 +164,7 @@ ATTN_CASES = [
     ("empty-ranks-fp8", [64, 200, 1], 64, 1, 8, "e4m3"),
     ("causal-q4-fp8", [64 * 7 + 3, 66, 260], 64, 4, 2, "e4m3"),
     ("heads-96-fp8", [700, 333], 96, 1, 3, "e4m3"),
-    # one long segment per rank (single-term FP8 P) next to short ones (hi + lo P)
+    # long segments per rank (chunked) next to short ones
     ("mixed-len-fp8", [70_000, 9_000], 64, 1, 8, "e4m3"),
     # the largest DCP size, 32 heads (half a query group), 128 heads (two groups) with q_len 2
     ("dcp16", [5000, 700, 1], 64, 1, 16, "bf16"),
