@@ -183,15 +183,17 @@ class Workload:
         self.lens = lens
         self.B = len(lens)
         counts = [e - s for s, e in (split(self.L, self.n_cp, r) for r in range(self.n_cp))]
-        # layer pipeline (several CP source ranks): the reshard runs per source rank on a stream
-        # of higher priority, and each layer's attention starts as soon as its rank's layers
-        # have arrived, so the attention of the first layers overlaps the transfer of the rest
+        # layer pipeline (several layers): the reshard runs layer by layer on a stream of higher
+        # priority (one call per layer, on the source rank's pool view of that layer), and each
+        # layer's attention starts as soon as its layer has arrived, so the attention of the
+        # first layers overlaps the transfer of the rest
         self.layer_rank = [r for r in range(self.n_cp) for _ in range(counts[r])]
+        self.layer_in_rank = [l - sum(counts[:self.layer_rank[l]]) for l in range(self.L)]
         self.layer_pipe = (overlap_layers and self.overlap_plan and not naive and staging_mb == 0
-                           and layout == "page" and self.n_cp > 1)
+                           and layout == "page" and self.L > 1)
         if self.layer_pipe:
             self.rs = torch.cuda.Stream(device, priority=-1)
-            self.rank_done = [torch.cuda.Event() for _ in range(self.n_cp)]
+            self.layer_done = [torch.cuda.Event() for _ in range(self.L)]
         self.rc = di.reshard_case(lens, n_layers=self.L, layer_counts=counts, n_dcp=self.N, dtype=self.dtype,
                                   contiguous_src=True, seed=seed, device=device, dst_slots=slots)
         self.q = di.random_q(self.B, self.T, self.H, di._gen(seed + 7, device), device)
@@ -240,7 +242,7 @@ class Workload:
         self.launches_per_step = (1 + self.L * 5 if not self.overlap_plan else
                                   3 + self.L * (4 if self.dtype == "e4m3" else 3))
         if self.layer_pipe:
-            self.launches_per_step += self.n_cp - 1  # one reshard launch per source rank
+            self.launches_per_step += self.L - 1  # one reshard launch per layer
         if self.naive:
             n_pages = self.rc.dst_vpages.numel()
             need = self.N * self.L * n_pages * self.rc.page_bytes
@@ -357,16 +359,15 @@ class Workload:
                           dev_error=self.err)
         self.rs.wait_stream(main)  # the previous step's attention is done with the destination pools
         with torch.cuda.stream(self.rs):
-            for r in range(self.n_cp):
-                dcp.reshard_pages(rc.req_page_ptr, rc.src_pages, rc.dst_vpages, self.L, src_pools,
-                                  rc.src_pool_pages, rc.dst_pools, rc.dst_slots, only_src_rank=r, dev_error=self.err)
-                self.rank_done[r].record(self.rs)
+            for l in range(self.L):
+                r = self.layer_rank[l]
+                dcp.reshard_pages(rc.req_page_ptr, rc.src_pages, rc.dst_vpages, 1, [src_pools[r][self.layer_in_rank[l]]],
+                                  rc.src_pool_pages, [p[l] for p in rc.dst_pools], rc.dst_slots, n_dcp=self.N,
+                                  dev_error=self.err)
+                self.layer_done[l].record(self.rs)
         main.wait_stream(self.side)
-        waited = -1
         for l in range(self.L):
-            if self.layer_rank[l] != waited:
-                waited = self.layer_rank[l]
-                main.wait_event(self.rank_done[waited])
+            main.wait_event(self.layer_done[l])
             dcp.decode_attn_merged(q, self.seq_lens, rc.req_page_ptr, rc.dst_vpages, self.layer_pools[l], self.scale,
                                    self.kv_scale, o_part=self.o_part, lse_part=self.lse_part, o_out=self.o[l],
                                    lse_out=self.lse[l], workspace=self.ws, dev_error=self.err, planned=True)
@@ -686,9 +687,9 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16" if wl.dtype == "bf16" else "e4m3 (fp32 accumulate)",
         "data": "synthetic",
         "config": workload_config(wl, world),
-        "schedule": ("layer pipeline: the reshard per CP source rank on a high-priority stream, each layer's "
-                     "attention as soon as its source rank's layers have arrived (the stage pass below runs "
-                     "the stages one after the other)" if wl.layer_pipe else "stages in order"),
+        "schedule": ("layer pipeline: the reshard layer by layer on a high-priority stream, each layer's "
+                     "attention as soon as its layer has arrived (the stage pass below runs the stages one "
+                     "after the other)" if wl.layer_pipe else "stages in order"),
         "stages": {
             "reshard": {"ms": stage_ms["reshard"], "GB/s": stage_gbs["reshard"], "frac_hbm": stage_gbs["reshard"] / hbm,
                         **({"mode": f"bounded pack, {args.staging_mb} MB staging buffer",
@@ -751,8 +752,8 @@ def main():
     ap.add_argument("--profile-steps", action="store_true",
                     help="run only the warm-up and --steps plain steps (for ncu captures; no bench line)")
     ap.add_argument("--no-layer-overlap", action="store_true",
-                    help="several CP source ranks: reshard all layers before the first attention instead of "
-                         "starting each layer's attention as soon as its source rank's layers have arrived")
+                    help="several layers: reshard all layers before the first attention instead of starting "
+                         "each layer's attention as soon as its layer has arrived")
     ap.add_argument("--unfused", action="store_true",
                     help="partial attention and the LSE merge as separate calls (default: one call)")
     args = ap.parse_args()

@@ -109,8 +109,8 @@ def test_reference_arm_under_torchrun_prints_once():
 
 @pytest.mark.gpu
 def test_layer_pipeline_equals_the_stages_in_order(cuda_device):
-    """The bench's layer pipeline (reshard per source rank on its own stream, each layer's
-    attention after its rank's layers) computes bit for bit what the stages in order compute."""
+    """The bench's layer pipeline (the reshard layer by layer on its own stream, each layer's
+    attention after its layer) computes bit for bit what the stages in order compute."""
     import torch
     sys.path.insert(0, ROOT)
     import bench
