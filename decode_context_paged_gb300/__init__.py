@@ -94,6 +94,8 @@ def _load():
         lib.dcp_partial_decode_attn_run.restype = i32
         lib.dcp_attn_plan.argtypes = [i32, i32, i32, vp, i64, vp, i32, i32, i64, i32, vp, sz, vp, vp]
         lib.dcp_attn_plan.restype = i32
+        lib.dcp_attn_plan_info.argtypes = [i32, i32, i32, i64, i32, i32, vp, sz, vp, vp]
+        lib.dcp_attn_plan_info.restype = i32
         lib.dcp_partial_decode_attn_static.argtypes = [i32, i32, i32, vp, vp, vp, i64, vp, i32, i32, f32, f32,
                                                        i32, vp, i64, i32, vp, vp, vp, vp]
         lib.dcp_partial_decode_attn_static.restype = i32
@@ -397,6 +399,20 @@ def attn_plan(q_shape: tuple, req_page_ptr: torch.Tensor, dst_vpages: torch.Tens
                                  kv_pools[0].shape[0], only_rank, _dptr(workspace, "workspace"), workspace.numel(),
                                  _dptr(dev_error, "dev_error", torch.int32), _stream(stream)),
            "dcp_attn_plan")
+
+
+def attn_plan_info(q_shape: tuple, num_pages: int, kv_pools: list, workspace: torch.Tensor, stream=None) -> dict:
+    """The header of the plan in ``workspace`` (dcp_attn_plan_info, synchronous): work units in
+    the queue, (rank, request) pairs split into several pieces, tiles per chunk, and whether the
+    workspace holds a plan at all."""
+    B, T, H = q_shape[:3]
+    _check_pools(kv_pools)
+    info = (ctypes.c_int32 * 4)()
+    _check(_load().dcp_attn_plan_info(B, T, H, int(num_pages), _kv_code(kv_pools[0]), len(kv_pools),
+                                      _dptr(workspace, "workspace"), workspace.numel(), ctypes.addressof(info),
+                                      _stream(stream)),
+           "dcp_attn_plan_info")
+    return {"units": info[0], "split_pairs": info[1], "tiles_per_chunk": info[2], "valid": bool(info[3])}
 
 
 def decode_attn_merged(q: torch.Tensor, seq_lens: torch.Tensor, req_page_ptr: torch.Tensor,

@@ -396,6 +396,19 @@ int dcp_attn_plan(int num_requests, int q_len, int num_heads, const int64_t *req
                              workspace_bytes, dev_error, stream, 0, 1);
 }
 
+int dcp_attn_plan_info(int num_requests, int q_len, int num_heads, int64_t num_pages, int dtype, int n_dcp,
+                       const void *workspace, size_t workspace_bytes, int32_t *info, dcp_stream_t stream) {
+    if (num_requests < 0 || q_len < 1 || num_heads < 1 || num_pages < 0 || !info) return DCP_ERR_INVALID_ARG;
+    if (dtype != DCP_KV_BF16 && dtype != DCP_KV_FP8_E4M3) return DCP_ERR_INVALID_ARG;
+    if (n_dcp < 1 || n_dcp > kMaxDcpAttn) return DCP_ERR_INVALID_ARG;
+    int sms = 0;
+    if (int st = current_sm_count(&sms)) return st;
+    AttnPlanShape s;
+    if (!plan_attention(num_requests, q_len, num_heads, n_dcp, num_pages, dtype, sms, &s)) return DCP_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < s.total_bytes || !aligned(workspace, 256)) return DCP_ERR_WORKSPACE;
+    return read_plan_info(s, workspace, info, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int dcp_partial_decode_attn_run(int num_requests, int q_len, int num_heads, const void *q, const int32_t *seq_lens,
                                 const int64_t *req_page_ptr, int64_t num_pages, const int32_t *dst_vpages,
                                 int page_size, int dtype, float kv_scale, float softmax_scale, int n_dcp,

@@ -1235,89 +1235,262 @@ __device__ void plan_scatter_tile(int b, int k, int N, long long num_pages, long
     }
 }
 
-// The last block of plan_build_kernel: chunk each (rank, request) pair, assign partial slots,
-// list the multi-chunk pairs, emit units largest first with the G query groups of a chunk
-// adjacent.
-__device__ void plan_build_units(int B, int N, int G, int only_rank, int tpc, unsigned long long key,
+// The last block of plan_build_kernel: chunk each (rank, request) pair, emit units largest first
+// with the G query groups of a chunk adjacent, cut the chunks of the queue's last, partly
+// filled round into pieces (below), assign partial slots and list the multi-piece pairs.
+//
+// Tail cut.  Persistent CTAs take units from the queue in order, so with U units of similar
+// size on P SMs the last U mod P of them run while the other SMs idle (48 requests x 8 ranks of
+// 98 tiles on 152 SMs: 80 SMs run a third unit after the others are done).  The chunks from the
+// first position of that round on -- the smallest, ties taken by the highest (request, rank,
+// chunk), so that the cut pairs gather in few requests and the other requests' rows merge
+// while the chunk partials combine -- are laid end to end in (size descending, request, rank,
+// chunk) order and cut at the multiples of
+// q = their work / P; each piece is a unit with a partial of its own (merged like chunks), and
+// the pieces take the tail of the queue largest first.  Which chunks are cut, where, and the
+// order of a pair's partials do not depend on thread timing, so results are reproducible.
+// Only where the largest of those chunks is well above q (a cut costs a partial's round trip
+// and a unit boundary, about three tiles) and the pieces fit the workspace.
+constexpr int kMinPiece = 8;
+constexpr int kMaxTailChunks = kPlanThreads;  // one thread per tail chunk in the sort and scans
+__device__ void plan_build_units(int B, int N, int G, int only_rank, int tpc, int num_sms, long long max_units,
+                                 long long max_partials, unsigned long long key,
                                  const int64_t *__restrict__ req_page_ptr,
                                  int tiles_per_req, const int32_t *__restrict__ tile_cnt, int32_t *__restrict__ counts,
                                  int32_t *__restrict__ pair_chunks, int32_t *__restrict__ pair_part,
                                  int32_t *__restrict__ multi_list, int4 *__restrict__ units, int *__restrict__ ctrl) {
-    __shared__ int hist[kMaxTpc + 1];
+    __shared__ int hist[kMaxTpc + 1];                    // chunks per size, then next queue position per size
+    __shared__ unsigned long long tkey[kMaxTailChunks];  // tail chunk: (kMaxTpc - size) << 32 | b * N + d
+    __shared__ int tchunk[kMaxTailChunks];               // tail chunk: chunk index within its pair
+    __shared__ int tpieces[kMaxTailChunks];
     __shared__ long long scratch[33];
-    __shared__ int n_multi;
+    __shared__ int n_multi, n_tail, n_extra, u_c, q_cut, tail_start, s_b, b_first;
+    __shared__ unsigned long long part_before;
     const int n_pair = N * B;
-    if (threadIdx.x == 0) n_multi = 0;
-    for (int pr = threadIdx.x; pr < n_pair; pr += blockDim.x) {  // per (rank, request) totals
+    const int tid = threadIdx.x;
+    auto active = [&](int pr) { return only_rank < 0 || pr / B == only_rank; };
+    auto n_chunks = [&](int tiles) { return tiles == 0 ? 1 : (tiles + tpc - 1) / tpc; };
+    auto chunk_size = [&](int tiles, int c) { return max(0, min(tpc, tiles - c * tpc)); };
+    if (tid == 0) {
+        n_multi = 0;
+        n_tail = 0;
+        n_extra = 0;
+        part_before = 0;
+    }
+    for (int i = tid; i <= tpc; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    for (int pr = tid; pr < n_pair; pr += blockDim.x) {  // per (rank, request): pages, chunks
         const int d = pr / B, b = pr % B;
         const long long np = req_page_ptr[b + 1] - req_page_ptr[b];
         const int nt = (int)((np + kPlanTile - 1) / kPlanTile);
         int acc = 0;
         for (int k = 0; k < nt; ++k) acc += tile_cnt[((long long)b * tiles_per_req + k) * kMaxDcpAttn + d];
         counts[pr] = acc;
-    }
-    for (int i = threadIdx.x; i <= tpc; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
-    long long running = 0;
-    for (int base = 0; base < n_pair; base += blockDim.x) {
-        const int pr = base + threadIdx.x;
-        int chunks = 0, tiles = 0;
-        if (pr < n_pair) {
-            const int d = pr / B;
-            if (only_rank < 0 || d == only_rank) {
-                tiles = (counts[pr] + 1) >> 1;
-                chunks = tiles == 0 ? 1 : (tiles + tpc - 1) / tpc;
-            }
-            pair_chunks[pr] = chunks;
-            if (chunks > 1) multi_list[atomicAdd(&n_multi, 1)] = pr;
+        int chunks = 0;
+        if (active(pr)) {
+            const int tiles = (acc + 1) >> 1;
+            chunks = n_chunks(tiles);
+            for (int c = 0; c < chunks; ++c) atomicAdd(&hist[chunk_size(tiles, c)], 1);
+            if (chunks > 1) atomicAdd(&part_before, (unsigned long long)chunks * G);
         }
-        long long tot;
-        const long long need = chunks > 1 ? (long long)chunks * G : 0;
-        const long long off = block_exclusive_scan(need, scratch, &tot);
-        if (pr < n_pair) pair_part[pr] = chunks > 1 ? (int)(running + off) : -1;
-        running += tot;
-        for (int c = 0; c < chunks; ++c) {
-            const int sz = min(tpc, tiles - c * tpc);
-            atomicAdd(&hist[sz < 0 ? 0 : sz], 1);
-        }
+        pair_chunks[pr] = chunks;  // grows by the pieces of cut chunks
     }
     __syncthreads();
-    if (threadIdx.x == 0) {  // bucket offsets, largest size first (in units of chunks)
+    if (tid == 0) {
+        // bucket starts, largest size first (positions in units of chunks)
         int acc = 0;
-        for (int s = tpc; s >= 0; --s) {
-            const int h = hist[s];
-            hist[s] = acc;
+        for (int sz = tpc; sz >= 0; --sz) {
+            const int h = hist[sz];
+            hist[sz] = acc;
             acc += h;
         }
-        ctrl[0] = acc * G;
+        u_c = acc;
+        int q = 0, ts = acc, sb = 0, first = 0;
+        const long long units_total = (long long)acc * G;
+        const long long full = units_total / num_sms;
+        if (full >= 1 && units_total % num_sms != 0) {
+            ts = (int)((full * num_sms + G - 1) / G);
+            long long s_tail = 0;
+            int smax = -1;
+            for (int sz = tpc; sz >= 0; --sz) {  // bucket sz holds positions [hist[sz], end)
+                const int b0 = hist[sz], b1 = sz > 0 ? hist[sz - 1] : acc;
+                if (b1 <= ts || b0 == b1) continue;
+                if (smax < 0) {  // the boundary bucket: its chunks of rank >= first are in the tail
+                    smax = sz;
+                    sb = sz;
+                    first = max(b0, ts) - b0;
+                }
+                s_tail += (long long)(b1 - max(b0, ts)) * sz;
+            }
+            const long long qq = (s_tail * G + num_sms - 1) / num_sms;
+            const long long cuts = qq > 0 ? s_tail / qq : 0;
+            const bool pays = qq >= kMinPiece && 4LL * smax > 5 * qq + 16;
+            const bool fits = acc - ts <= kMaxTailChunks && units_total + cuts * G <= max_units &&
+                              (long long)part_before + (cuts + (acc - ts)) * G <= max_partials;
+            if (pays && fits) q = (int)qq;
+        }
+        q_cut = q;
+        tail_start = q > 0 ? ts : acc;
+        s_b = sb;
+        b_first = first;
+    }
+    __syncthreads();
+    const int q = q_cut, ts = tail_start, uc = u_c, sb = s_b;
+    // (request, rank, chunk) rank of each pair's first chunk of size sb among all chunks of that
+    // size (kept in pair_part until the partial slots are assigned)
+    if (q > 0) {
+        long long running = 0;
+        for (int base = 0; base < n_pair; base += blockDim.x) {
+            const int idx = base + tid;  // request-major
+            const int pr = idx < n_pair ? (idx % N) * B + idx / N : n_pair;
+            int x = 0;
+            if (pr < n_pair && active(pr)) {
+                const int tiles = (counts[pr] + 1) >> 1;
+                if (tiles == 0) x = sb == 0;
+                else x = (sb == tpc ? tiles / tpc : 0) + (tiles % tpc != 0 && tiles % tpc == sb);
+            }
+            long long tot;
+            const long long off = block_exclusive_scan(x, scratch, &tot);
+            if (pr < n_pair) pair_part[pr] = (int)(running + off);
+            running += tot;
+        }
+    }
+    __syncthreads();
+    for (int pr = tid; pr < n_pair; pr += blockDim.x) {
+        if (!active(pr)) continue;
+        const int cnt = counts[pr];
+        const int tiles = (cnt + 1) >> 1;
+        const int chunks = n_chunks(tiles);
+        for (int c = 0; c < chunks; ++c) {
+            const int sz = chunk_size(tiles, c);
+            const bool in_tail = q > 0 && (sz < sb || (sz == sb && pair_part[pr] + (sz == tpc ? c : 0) >= b_first));
+            if (in_tail) {
+                const int j = atomicAdd(&n_tail, 1);
+                tkey[j] = ((unsigned long long)(kMaxTpc - sz) << 32) | (unsigned)((pr % B) * N + pr / B);
+                tchunk[j] = c;
+                continue;
+            }
+            const int pos = atomicAdd(&hist[sz], 1);
+            const int page_begin = c * 2 * tpc;
+            const int n_pages = max(0, min(2 * tpc, cnt - page_begin));
+            for (int g = 0; g < G; ++g) units[(long long)pos * G + g] = make_int4(pr * G + g, page_begin, n_pages, c);
+        }
+    }
+    __syncthreads();
+    if (q > 0) {
+        const int nt = n_tail;  // == uc - ts
+        if (tid >= nt) {
+            tkey[tid] = ~0ull;
+            tchunk[tid] = 0x7fffffff;
+        }
+        __syncthreads();
+        for (int k = 2; k <= kMaxTailChunks; k <<= 1) {  // bitonic sort by (key, chunk)
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                const int l = tid ^ j;
+                if (l > tid) {
+                    const unsigned long long ka = tkey[tid], kb = tkey[l];
+                    const int ca = tchunk[tid], cb = tchunk[l];
+                    const bool gt = ka > kb || (ka == kb && ca > cb);
+                    if (gt == ((tid & k) == 0)) {
+                        tkey[tid] = kb;
+                        tkey[l] = ka;
+                        tchunk[tid] = cb;
+                        tchunk[l] = ca;
+                    }
+                }
+                __syncthreads();
+            }
+        }
+        // end-to-end offsets, pieces: cuts at the multiples of q strictly inside [o, o + size)
+        const bool mine = tid < nt;
+        const int bn = mine ? (int)(tkey[tid] & 0xffffffffu) : 0;
+        const int pr = (bn % N) * B + bn / N;
+        const int sz = mine ? kMaxTpc - (int)(tkey[tid] >> 32) : 0;
+        const int c = mine ? tchunk[tid] : 0;
+        long long tot;
+        const int o = (int)block_exclusive_scan(sz, scratch, &tot);
+        const int m0 = o / q;
+        const int k = (mine && sz > 0) ? (o + sz - 1) / q - m0 + 1 : 1;
+        tpieces[tid] = k;
+        for (int i = tid; i <= tpc; i += blockDim.x) hist[i] = 0;
+        __syncthreads();
+        int first = 0;  // partial ordinal of this chunk's second piece: after the pair's chunks and
+                        // the extra pieces of its tail chunks of lower index
+        if (mine) {
+            first = n_chunks((counts[pr] + 1) >> 1);
+            for (int j = 0; j < nt; ++j)
+                if ((int)(tkey[j] & 0xffffffffu) == bn && tchunk[j] < c) first += tpieces[j] - 1;
+            if (k > 1) {
+                atomicAdd(&pair_chunks[pr], k - 1);
+                atomicAdd(&n_extra, k - 1);
+            }
+            for (int i = 0; i < k; ++i) {
+                const int t0 = i == 0 ? 0 : (m0 + i) * q - o;
+                const int t1 = i == k - 1 ? sz : (m0 + i + 1) * q - o;
+                atomicAdd(&hist[t1 - t0], 1);
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {  // the pieces fill the queue from position ts, largest first
+            int acc = ts;
+            for (int s2 = tpc; s2 >= 0; --s2) {
+                const int h = hist[s2];
+                hist[s2] = acc;
+                acc += h;
+            }
+        }
+        __syncthreads();
+        if (mine) {
+            const int cnt = counts[pr];
+            const int page_begin = c * 2 * tpc;
+            const int n_pages = max(0, min(2 * tpc, cnt - page_begin));
+            for (int i = 0; i < k; ++i) {
+                const int t0 = i == 0 ? 0 : (m0 + i) * q - o;
+                const int t1 = i == k - 1 ? sz : (m0 + i + 1) * q - o;
+                const int pb = page_begin + 2 * t0;
+                const int np = max(0, min(page_begin + n_pages, page_begin + 2 * t1) - pb);
+                const long long at = atomicAdd(&hist[t1 - t0], 1);
+                const int ordinal = i == 0 ? c : first + i - 1;
+                for (int g = 0; g < G; ++g) units[at * G + g] = make_int4(pr * G + g, pb, np, ordinal);
+            }
+        }
+    }
+    __syncthreads();
+    // partial slots of the multi-piece pairs
+    long long running = 0;
+    for (int base = 0; base < n_pair; base += blockDim.x) {
+        const int pr = base + tid;
+        const int pieces = pr < n_pair ? pair_chunks[pr] : 0;
+        long long tot;
+        const long long need = pieces > 1 ? (long long)pieces * G : 0;
+        const long long off = block_exclusive_scan(need, scratch, &tot);
+        if (pr < n_pair) {
+            pair_part[pr] = pieces > 1 ? (int)(running + off) : -1;
+            if (pieces > 1) multi_list[atomicAdd(&n_multi, 1)] = pr;
+        }
+        running += tot;
+    }
+    __syncthreads();
+    const long long n_units = (long long)(uc + n_extra) * G;
+    for (long long i = tid; i < n_units; i += blockDim.x) {  // ordinal -> partial slot
+        int4 r = units[i];
+        const int pr = r.x / G, g = r.x - pr * G;
+        r.w = pair_part[pr] >= 0 ? pair_part[pr] + r.w * G + g : -1;
+        units[i] = r;
+    }
+    if (tid == 0) {
+        ctrl[0] = (int)n_units;
         ctrl[1] = 0;
         ctrl[2] = n_multi;
         ctrl[3] = kPlanMagic;
         *reinterpret_cast<unsigned long long *>(ctrl + 4) = key;
         *reinterpret_cast<long long *>(ctrl + 6) = (long long)req_page_ptr[B];
     }
-    __syncthreads();
-    for (int pr = threadIdx.x; pr < n_pair; pr += blockDim.x) {
-        const int chunks = pair_chunks[pr];
-        if (chunks == 0) continue;
-        const int tiles = (counts[pr] + 1) >> 1;
-        const int cnt = counts[pr];
-        for (int c = 0; c < chunks; ++c) {
-            const int sz = max(0, min(tpc, tiles - c * tpc));
-            const int slot = atomicAdd(&hist[sz], 1);
-            const int page_begin = c * 2 * tpc;
-            const int n_pages = max(0, min(2 * tpc, cnt - page_begin));
-            for (int g = 0; g < G; ++g) {
-                const int out = chunks > 1 ? pair_part[pr] + c * G + g : -1;
-                units[(long long)slot * G + g] =
-                    make_int4(pr * G + g, page_begin, n_pages, out);
-            }
-        }
-    }
 }
 
 __global__ void __launch_bounds__(kPlanThreads)
-plan_build_kernel(int B, int N, int G, int only_rank, int tpc, unsigned long long key, long long num_pages,
+plan_build_kernel(int B, int N, int G, int only_rank, int tpc, int num_sms, long long max_units, long long max_partials,
+                  unsigned long long key, long long num_pages,
                   long long slots_per_rank,
                   int tiles_per_req, int tile_stride, const int64_t *__restrict__ req_page_ptr, const int32_t *__restrict__ vpages,
                   const int32_t *__restrict__ tile_cnt, int32_t *__restrict__ comp_slot, int32_t *__restrict__ comp_page,
@@ -1333,7 +1506,8 @@ plan_build_kernel(int B, int N, int G, int only_rank, int tpc, unsigned long lon
             plan_scatter_tile(b, k, N, num_pages, slots_per_rank, tiles_per_req, req_page_ptr, vpages, tile_cnt,
                               comp_slot, comp_page);
     } else
-        plan_build_units(B, N, G, only_rank, tpc, key, req_page_ptr, tiles_per_req, tile_cnt, counts, pair_chunks,
+        plan_build_units(B, N, G, only_rank, tpc, num_sms, max_units, max_partials, key, req_page_ptr, tiles_per_req,
+                         tile_cnt, counts, pair_chunks,
                          pair_part, multi_list, units, ctrl);
 }
 
@@ -1369,9 +1543,18 @@ __global__ void combine_kernel(int B, int T, int H, int HB, int G, int *ctrl, un
     }
 }
 
-// Fused merge, first launch after the attention kernel.  With no multi-chunk pair (ctrl[2] ==
-// 0) it merges every row over the ranks, one warp per row, ascending rank order.  Otherwise it combines the chunk partials as combine_kernel does
-// and leaves the rank merge to merge_after_combine_kernel.
+// Whether any rank's segment of request b was split into several pieces (warp-uniform: lane d
+// reads rank d's piece count).
+__device__ __forceinline__ bool request_split(int b, int B, int N, const int32_t *__restrict__ pair_chunks) {
+    const int lane = threadIdx.x & 31;
+    const bool split = lane < N && __ldg(pair_chunks + (long long)lane * B + b) > 1;
+    return __any_sync(0xffffffffu, split);
+}
+
+// Fused merge, first launch after the attention kernel: one warp per task.  It combines the
+// chunk partials of the multi-piece pairs (as combine_kernel does) and merges over the ranks,
+// ascending rank order, the rows of the requests none of whose pairs was split; the rows of
+// the other requests are merged by merge_after_combine_kernel.
 __global__ void merge_combine_kernel(int B, int T, int H, int HB, int G, int N, int *ctrl, unsigned long long key,
                                      const int64_t *__restrict__ req_page_ptr,
                                      const int32_t *__restrict__ multi_list, const int32_t *__restrict__ pair_chunks,
@@ -1384,10 +1567,16 @@ __global__ void merge_combine_kernel(int B, int T, int H, int HB, int G, int N, 
     if (blockIdx.x == 0 && threadIdx.x == 0) ctrl[1] = 0;  // the work counter, ready for the next run of the plan
     const int n_multi = ctrl[2];
     const int wpb = blockDim.x >> 5;
-    if (n_multi > 0) {
-        const long long n_tasks = (long long)n_multi * G * kGroupRows;
-        for (long long task = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); task < n_tasks;
-             task += (long long)gridDim.x * wpb) {
+    const long long n_comb = (long long)n_multi * G * kGroupRows;
+    const long long rows = (long long)B * T * H;
+    for (long long task = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); task < n_comb + rows;
+         task += (long long)gridDim.x * wpb) {
+        // one call site for both kinds of task (registers): n parts at o / lse with strides
+        int n;
+        const float *o, *lse;
+        long long o_stride, lse_stride;
+        float *dst, *dst_lse;
+        if (task < n_comb) {
             const int c = (int)(task % kGroupRows);
             const long long pg = task / kGroupRows;
             const int g = (int)(pg % G);
@@ -1397,30 +1586,44 @@ __global__ void merge_combine_kernel(int B, int T, int H, int HB, int G, int N, 
             const int d = pr / B, b = pr % B;
             const long long first = (long long)pair_part[pr] + g;
             const long long out_row = (long long)d * B * T * H + ((long long)(b * T + t) * H) + hb * kGroupRows + c;
-            warp_merge_row512(pair_chunks[pr], part_o + (first * kGroupRows + c) * kVDim,
-                              (long long)G * kGroupRows * kVDim, part_lse + first * kGroupRows + c,
-                              (long long)G * kGroupRows, o_part + out_row * kVDim, lse_part + out_row, 1.f);
+            n = pair_chunks[pr];
+            o = part_o + (first * kGroupRows + c) * kVDim;
+            o_stride = (long long)G * kGroupRows * kVDim;
+            lse = part_lse + first * kGroupRows + c;
+            lse_stride = (long long)G * kGroupRows;
+            dst = o_part + out_row * kVDim;
+            dst_lse = lse_part + out_row;
+        } else {
+            const long long row = task - n_comb;
+            if (n_multi > 0 && request_split((int)row / (T * H), B, N, pair_chunks)) continue;  // rows < 2^31
+            n = N;
+            o = o_part + row * kVDim;
+            o_stride = rows * kVDim;
+            lse = lse_part + row;
+            lse_stride = rows;
+            dst = o_out + row * kVDim;
+            dst_lse = lse_out + row;
         }
-        return;
+        warp_merge_row512(n, o, o_stride, lse, lse_stride, dst, dst_lse, 1.f);
     }
-    const long long rows = (long long)B * T * H;
-    for (long long row = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * wpb)
-        warp_merge_row512(N, o_part + row * kVDim, rows * kVDim, lse_part + row, rows, o_out + row * kVDim,
-                          lse_out + row, 1.f);
 }
 
-// Fused merge, second launch: the rank merge of every row when merge_combine_kernel combined
-// chunk partials instead (ctrl[2] > 0); exits at once otherwise.
-__global__ void merge_after_combine_kernel(int N, long long rows, const int *__restrict__ ctrl, unsigned long long key,
-                                           const int64_t *__restrict__ req_page_ptr, int B, const float *o_part,
+// Fused merge, second launch: the rank merge of the rows of the requests with a split pair,
+// after merge_combine_kernel has combined their chunk partials; exits at once when there are
+// none (ctrl[2] == 0).
+__global__ void merge_after_combine_kernel(int N, long long rows, int TH, const int *__restrict__ ctrl,
+                                           unsigned long long key, const int64_t *__restrict__ req_page_ptr, int B,
+                                           const int32_t *__restrict__ pair_chunks, const float *o_part,
                                            const float *lse_part, float *o_out, float *lse_out) {
     grid_dep_wait();
     grid_dep_launch();
     if (!plan_matches(ctrl, key, req_page_ptr, B) || ctrl[2] == 0) return;
     const int wpb = blockDim.x >> 5;
-    for (long long row = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * wpb)
+    for (long long row = (long long)blockIdx.x * wpb + (threadIdx.x >> 5); row < rows; row += (long long)gridDim.x * wpb) {
+        if (!request_split((int)row / TH, B, N, pair_chunks)) continue;  // rows < 2^31
         warp_merge_row512(N, o_part + row * kVDim, rows * kVDim, lse_part + row, rows, o_out + row * kVDim,
                           lse_out + row, 1.f);
+    }
 }
 
 // ------------------------------------------------------------------------ tensor maps
@@ -1556,6 +1759,20 @@ int launch_kernel(const AttnMaps &maps, const KParams &kp, int grid, cudaStream_
                ? DCP_OK : DCP_ERR_CUDA;
 }
 
+int read_plan_info(const AttnPlanShape &s, const void *workspace, int32_t *info, cudaStream_t stream) {
+    int ctrl[8];
+    const uint8_t *ws = static_cast<const uint8_t *>(workspace);
+    if (cudaMemcpyAsync(ctrl, ws + s.off_ctrl, sizeof(ctrl), cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess)
+        return DCP_ERR_CUDA;
+    const bool valid = ctrl[3] == kPlanMagic;
+    info[0] = valid ? ctrl[0] : 0;
+    info[1] = valid ? ctrl[2] : 0;
+    info[2] = s.tiles_per_chunk;
+    info[3] = valid ? 1 : 0;
+    return DCP_OK;
+}
+
 int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     const AttnPlanShape &s = a.shape;
     const bool f8 = a.dtype == DCP_KV_FP8_E4M3;
@@ -1591,7 +1808,7 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
         return DCP_ERR_CUDA;
     if (a.phase != 2 &&
         launch_pdl(plan_build_kernel, dim3(n_tile_blocks + 1), dim3(kPlanThreads), 0, stream, s.B, s.N, s.G,
-                   a.only_rank, s.tiles_per_chunk, key, (long long)s.num_pages, (long long)a.slots_per_rank, s.tiles_per_req,
+                   a.only_rank, s.tiles_per_chunk, num_sms, (long long)s.max_units, (long long)s.max_partials, key, (long long)s.num_pages, (long long)a.slots_per_rank, s.tiles_per_req,
                    tile_stride, a.req_page_ptr, a.dst_vpages, (const int32_t *)tile_cnt, comp_slot, comp_page, counts, pair_chunks,
                    pair_part, multi_list, units, ctrl) != cudaSuccess)
         return DCP_ERR_CUDA;
@@ -1645,7 +1862,7 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
     if (st != DCP_OK) return st;
     if (a.o_out) {  // fused merge (see merge_combine_kernel)
         const long long rows = (long long)s.B * s.T * s.H;
-        const long long tasks = std::max<long long>(rows, (long long)s.N * s.B * s.G * kGroupRows);
+        const long long tasks = rows + (long long)s.N * s.B * s.G * kGroupRows;  // rank merges + chunk combines
         const int blocks = (int)std::max<long long>(1, std::min<long long>((tasks + 7) / 8, 8LL * num_sms));
         if (launch_pdl(merge_combine_kernel, dim3(blocks), dim3(256), 0, stream, s.B, s.T, s.H, kp.HB, s.G, s.N,
                        ctrl, key, a.req_page_ptr, (const int32_t *)multi_list, (const int32_t *)pair_chunks,
@@ -1653,9 +1870,9 @@ int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream) {
                        a.lse_part, a.o_out, a.lse_out) != cudaSuccess)
             return DCP_ERR_CUDA;
         const int mblocks = (int)std::max<long long>(1, std::min<long long>((rows + 7) / 8, 8LL * num_sms));
-        if (launch_pdl(merge_after_combine_kernel, dim3(mblocks), dim3(256), 0, stream, s.N, rows,
-                       (const int *)ctrl, key, a.req_page_ptr, s.B, (const float *)a.o_part, (const float *)a.lse_part, a.o_out,
-                       a.lse_out) != cudaSuccess)
+        if (launch_pdl(merge_after_combine_kernel, dim3(mblocks), dim3(256), 0, stream, s.N, rows, s.T * s.H,
+                       (const int *)ctrl, key, a.req_page_ptr, s.B, (const int32_t *)pair_chunks,
+                       (const float *)a.o_part, (const float *)a.lse_part, a.o_out, a.lse_out) != cudaSuccess)
             return DCP_ERR_CUDA;
         return DCP_OK;
     }

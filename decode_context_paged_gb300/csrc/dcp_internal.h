@@ -156,5 +156,9 @@ struct AttnArgs {
     uint64_t wait_limit_ns;
 };
 int launch_attention(const AttnArgs &a, int num_sms, cudaStream_t stream);
+// Reads the plan header of a workspace laid out as `s` (synchronous on `stream`): info[0] units
+// in the queue, info[1] pairs with several pieces, info[2] tiles per chunk, info[3] 1 if the
+// workspace holds a plan.
+int read_plan_info(const AttnPlanShape &s, const void *workspace, int32_t *info, cudaStream_t stream);
 
 }  // namespace dcp

@@ -328,6 +328,15 @@ int dcp_attn_plan(int num_requests, int q_len, int num_heads, const int64_t *req
                   int64_t num_pages, const int32_t *dst_vpages, int dtype, int n_dcp,
                   int64_t slots_per_rank, int only_rank, void *workspace, size_t workspace_bytes,
                   int32_t *dev_error, dcp_stream_t stream);
+/* Diagnostics: the header of the plan held by `workspace` (made by dcp_attn_plan or by any
+ * attention call on it, for these sizes, dtype and n_dcp), read synchronously on `stream`.
+ * info (HOST int32[4]): [0] work units in the queue, [1] (rank, request) pairs split into
+ * several pieces (chunks of a long segment, or pieces of the queue's last, partly filled round,
+ * which the plan cuts so that every SM stays busy to the end), [2] tiles of 128 tokens per chunk,
+ * [3] 1 if the workspace holds a plan, else 0 (and [0], [1] are 0).  Returns
+ * DCP_ERR_INVALID_ARG, DCP_ERR_WORKSPACE, DCP_ERR_CUDA. */
+int dcp_attn_plan_info(int num_requests, int q_len, int num_heads, int64_t num_pages, int dtype, int n_dcp,
+                       const void *workspace, size_t workspace_bytes, int32_t *info, dcp_stream_t stream);
 int dcp_partial_decode_attn_run(int num_requests, int q_len, int num_heads, const void *q,
                                 const int32_t *seq_lens, const int64_t *req_page_ptr,
                                 int64_t num_pages, const int32_t *dst_vpages, int page_size,

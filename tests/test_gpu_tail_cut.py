@@ -1,0 +1,128 @@
+"""GPU: the plan's tail cut.  Persistent CTAs take units largest first; when the last round of
+the queue is only partly filled, the plan cuts the chunks of that round into pieces of about
+(their work / number of SMs) tiles, merged like chunks.  The unit counts the device plan reports
+(dcp_attn_plan_info) must equal a host restatement of that rule, and the results must match the
+oracle on every rank whether or not a segment was cut."""
+import numpy as np
+import pytest
+import torch
+
+import dcp_inputs as di
+import decode_context_paged_gb300 as dcp
+from _parity import compare, oracle_attention, pool_bytes, q_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _pair_tiles(case):
+    """128-token tiles of every (rank, request) pair, rank-major (pair = d * B + b)."""
+    ptr = case.req_page_ptr.cpu().numpy()
+    own = (case.dst_vpages.cpu().numpy() % case.n_dcp) if case.n_dcp > 1 else np.zeros(int(ptr[-1]), np.int64)
+    tiles = []
+    for d in range(case.n_dcp):
+        for b in range(case.B):
+            pages = int((own[ptr[b]:ptr[b + 1]] == d).sum())
+            tiles.append((pages + 1) // 2)
+    return tiles
+
+
+def _expected(case, tpc, sms):
+    """(units, pairs with several pieces) by the rule the plan applies (host restatement)."""
+    G = case.T * ((case.H + 63) // 64)
+    chunks = [1 if t == 0 else -(-t // tpc) for t in _pair_tiles(case)]
+    sizes = []
+    for t, c in zip(_pair_tiles(case), chunks):
+        sizes += [max(0, min(tpc, t - k * tpc)) for k in range(c)]
+    multi_before = sum(1 for c in chunks if c > 1)
+    part_before = sum(c * G for c in chunks if c > 1)
+    n_pages = int(case.req_page_ptr[-1])
+    n_pair = case.n_dcp * case.B
+    max_partials = (G * (n_pages + n_pair)) // tpc + G
+    max_units = n_pair * G + max_partials
+    u_c = len(sizes)
+    total = u_c * G
+    full = total // sms
+    if full < 1 or total % sms == 0:
+        return total, multi_before
+    ts = -(-(full * sms) // G)
+    tail = sorted(sizes, reverse=True)[ts:]
+    s_tail, smax = sum(tail), (tail[0] if tail else 0)
+    q = -(-(s_tail * G) // sms)
+    cuts = s_tail // q if q else 0
+    pays = q >= 8 and 4 * smax > 5 * q + 16
+    fits = (u_c - ts <= 512 and total + cuts * G <= max_units and part_before + (cuts + u_c - ts) * G <= max_partials)
+    if not (pays and fits):
+        return total, multi_before
+    extra, cut_chunks, o = 0, 0, 0
+    for sz in tail:
+        k = (o + sz - 1) // q - o // q + 1 if sz > 0 else 1
+        extra += k - 1
+        cut_chunks += k > 1
+        o += sz
+    assert multi_before == 0, "the cases below have one chunk per pair"
+    return (u_c + extra) * G, cut_chunks
+
+
+def _plan(case):
+    ws = dcp.alloc_workspace(case.B, case.T, case.H, case.n_dcp, case.dst_vpages.numel(), case.q.device)
+    err = torch.zeros(1, dtype=torch.int32, device=case.q.device)
+    dcp.attn_plan((case.B, case.T, case.H), case.req_page_ptr, case.dst_vpages, case.pools, ws, dev_error=err)
+    info = dcp.attn_plan_info((case.B, case.T, case.H), case.dst_vpages.numel(), case.pools, ws)
+    assert int(err.item()) == 0 and info["valid"]
+    return ws, info
+
+
+def _cut_case(device, sms):
+    """ceil(SMs / 4.8) + 8 requests x 81,920 tokens at DCP=8: 80-tile segments, enough of them
+    (at least SMs / 0.6) that the plan keeps each whole, and a partly filled last round (16 of
+    320 units past it on 152 SMs) that the rule cuts."""
+    B = -(-sms * 10 // 48) + 8
+    return di.attention_case([81_920] * B, H=64, T=1, n_dcp=8, dtype="e4m3", slots_per_rank=None, seed=41,
+                             device=device, name=f"tail-cut-{B}x81920-fp8-dcp8")
+
+
+def test_plan_info_on_a_workspace_without_a_plan(cuda_device):
+    case = di.attention_case([1000, 300], H=64, T=1, n_dcp=4, dtype="bf16", slots_per_rank=None, seed=2,
+                             device=cuda_device)
+    ws = dcp.alloc_workspace(case.B, case.T, case.H, case.n_dcp, case.dst_vpages.numel(), cuda_device)
+    ws.zero_()
+    info = dcp.attn_plan_info((case.B, case.T, case.H), case.dst_vpages.numel(), case.pools, ws)
+    assert info["valid"] is False and info["units"] == 0 and info["split_pairs"] == 0
+
+
+def test_tail_cut_counts_and_parity(cuda_device):
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    case = _cut_case(cuda_device, sms)
+    ws, info = _plan(case)
+    units, split = _expected(case, info["tiles_per_chunk"], sms)
+    assert split > 0, "the case is built so that the rule cuts"
+    assert (info["units"], info["split_pairs"]) == (units, split)
+    # planned run and one-call run: partials of every rank and the merged output vs the oracle
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    args = (case.q, case.seq_lens, case.req_page_ptr, case.dst_vpages, case.pools, case.softmax_scale, case.kv_scale)
+    om, lm, o, l = dcp.decode_attn_merged(*args, workspace=ws, dev_error=err, planned=True)
+    o1, l1 = dcp.partial_decode_attn(*args, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(o, o1) and torch.equal(l, l1)
+    o, l, om, lm = (t.cpu().numpy() for t in (o, l, om, lm))
+    # two heads of every request: every pair (rank, request) is checked, cut or not
+    rows = np.array([b * case.H + h for b in range(case.B) for h in (b % 64, 63 - b % 64)], np.int64)
+    qb, pools = q_bits(case), pool_bytes(case)
+    for d in range(case.n_dcp):
+        ro, rl = oracle_attention(case, rank=d, rows=rows, qb=qb, pools=pools)
+        compare(o[d].reshape(-1, 512)[rows], l[d].reshape(-1)[rows], ro, rl, f"{case.name} rank {d}")
+    ro, rl = oracle_attention(case, rows=rows, qb=qb, pools=pools)
+    compare(om.reshape(-1, 512)[rows], lm.reshape(-1)[rows], ro, rl, f"{case.name} merged")
+
+
+@pytest.mark.parametrize("name", ["agent", "batch"])
+def test_tail_cut_rule_on_the_workloads(cuda_device, name):
+    """The agent workload (384 equal segments) is cut on a 152-SM GB300; the batch workload's
+    8-tile segments are not (a cut would cost more than it saves)."""
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    case = di.agent_case(cuda_device) if name == "agent" else di.batch_case(cuda_device)
+    _, info = _plan(case)
+    assert (info["units"], info["split_pairs"]) == _expected(case, info["tiles_per_chunk"], sms)
+    if sms == 152:
+        assert (info["split_pairs"] > 0) == (name == "agent")
