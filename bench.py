@@ -50,15 +50,16 @@ L2_BYTES = 129 << 20  # GB300 L2
 # on (for the reshard: dcp_reshard.cu and the copy ring header); a changed source reports
 # traffic null until it is re-measured.
 NCU_TRAFFIC = {
-    # (kernel, workload): (source hash, DRAM bytes per launch).  Captures on smaller cases of the
-    # same kernel (the agent8 / long1 configs, and agent8's reshard on the long-copy grid) are
-    # scaled by the units processed: pages for the reshard, requests for the attention.
+    # (kernel, workload): (source hash, DRAM bytes per launch).  The agent attention and the
+    # batch kernels are captured on their own workload; the others on smaller cases of the same
+    # kernel (the long1 config, and agent8's reshard on the long-copy grid), scaled by the units
+    # processed: pages for the reshard, requests for the attention.
     ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("26b6b9b40d4d64dd", 552448000),
     ("reshard_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("26b6b9b40d4d64dd", 5236858368),
     ("reshard_kernel", "e2e-64x463936-h64-q1-e4m3-dcp8-L8-cp4"): ("26b6b9b40d4d64dd", 44745598653),
-    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("12f2a36df02d7ace", 325443072),
-    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("12f2a36df02d7ace", 2799823872),
-    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("12f2a36df02d7ace", 2531567616),
+    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("38b2412f1ae73e47", 325671936),
+    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("38b2412f1ae73e47", 2791719680),
+    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("38b2412f1ae73e47", 2528733184),
 }
 
 
