@@ -72,13 +72,14 @@ def _plan(case):
     return ws, info
 
 
-def _cut_case(device, sms):
-    """ceil(SMs / 4.8) + 8 requests x 81,920 tokens at DCP=8: 80-tile segments, enough of them
-    (at least SMs / 0.6) that the plan keeps each whole, and a partly filled last round (16 of
-    320 units past it on 152 SMs) that the rule cuts."""
-    B = -(-sms * 10 // 48) + 8
-    return di.attention_case([81_920] * B, H=64, T=1, n_dcp=8, dtype="e4m3", slots_per_rank=None, seed=41,
-                             device=device, name=f"tail-cut-{B}x81920-fp8-dcp8")
+def _cut_case(device, sms, T=1):
+    """(ceil(SMs / 4.8) + 8) / q_len requests x 81,920 tokens at DCP=8: 80-tile segments, enough
+    units (at least SMs / 0.6) that the plan keeps each segment whole, and a partly filled last
+    round (16 of 320 units past it on 152 SMs) that the rule cuts.  With q_len 2 every chunk is
+    two units (the query groups of the two new tokens), cut alike."""
+    B = -(-sms * 10 // (48 * T)) + 8 // T
+    return di.attention_case([81_920] * B, H=64, T=T, n_dcp=8, dtype="e4m3", slots_per_rank=None, seed=41 + T,
+                             device=device, name=f"tail-cut-{B}x81920-q{T}-fp8-dcp8")
 
 
 def test_plan_info_on_a_workspace_without_a_plan(cuda_device):
@@ -90,9 +91,10 @@ def test_plan_info_on_a_workspace_without_a_plan(cuda_device):
     assert info["valid"] is False and info["units"] == 0 and info["split_pairs"] == 0
 
 
-def test_tail_cut_counts_and_parity(cuda_device):
+@pytest.mark.parametrize("T", [1, 2])
+def test_tail_cut_counts_and_parity(cuda_device, T):
     sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
-    case = _cut_case(cuda_device, sms)
+    case = _cut_case(cuda_device, sms, T)
     ws, info = _plan(case)
     units, split = _expected(case, info["tiles_per_chunk"], sms)
     assert split > 0, "the case is built so that the rule cuts"
@@ -106,8 +108,10 @@ def test_tail_cut_counts_and_parity(cuda_device):
     assert int(err.item()) == 0
     assert torch.equal(o, o1) and torch.equal(l, l1)
     o, l, om, lm = (t.cpu().numpy() for t in (o, l, om, lm))
-    # two heads of every request: every pair (rank, request) is checked, cut or not
-    rows = np.array([b * case.H + h for b in range(case.B) for h in (b % 64, 63 - b % 64)], np.int64)
+    # two heads of every request and new token: every (rank, request, query group) is checked,
+    # cut or not
+    rows = np.array([(b * case.T + t) * case.H + h for b in range(case.B) for t in range(case.T)
+                     for h in (b % 64, 63 - b % 64)], np.int64)
     qb, pools = q_bits(case), pool_bytes(case)
     for d in range(case.n_dcp):
         ro, rl = oracle_attention(case, rank=d, rows=rows, qb=qb, pools=pools)
