@@ -11,7 +11,7 @@
 //    cuts it into chunks of `tiles_per_chunk` 128-token tiles; a work unit is (rank,
 //    request, chunk, query group), a query group being one new token and up to 64 heads.
 //    Units are ordered by size (largest first) with the groups of one chunk adjacent, and
-//    persistent CTAs (one per SM) take them from an atomic counter.
+//    persistent CTAs (one per SM) take them from an atomic counter (CTA i starts with unit i).
 //  * Tokens are the MMA's M dimension (128 = two pages), query rows its N.  Per tile
 //    tcgen05 computes S^T[128 x n] = K_tile * Q^T into TMEM, the softmax warps turn it into
 //    P^T in shared memory, and tcgen05 accumulates O^T[512 x 64] += V_tile^T * P^T in TMEM.
@@ -414,6 +414,10 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
     grid_dep_wait();  // the plan (and the FP8 Q split) of this call
     grid_dep_launch();
     const uint32_t tmem = ctl->tmem_base;
+    // CTA i's first unit is unit i (the queue's first round gives every CTA one unit): its record
+    // is read while the plan is checked, and the atomic counter serves the later units only.
+    int4 first_rec = make_int4(0, 0, 0, 0);
+    if (warp == 0 && lane == 0) first_rec = p.units[blockIdx.x];  // in bounds: grid <= the unit capacity
     const bool plan_ok = plan_matches(p.ctrl, p.plan_key, p.req_page_ptr, p.B);
     if (!plan_ok && blockIdx.x == 0 && threadIdx.x == 0 && p.dev_error) atomicOr(p.dev_error, DCP_DEVERR_PLAN_MISMATCH);
     const int n_units = plan_ok ? p.ctrl[0] : 0;
@@ -481,11 +485,12 @@ attn_kernel(const __grid_constant__ AttnMaps maps, const __grid_constant__ KPara
                     ok = false;
                     break;
                 }
-                const int idx = n_units > 0 ? atomicAdd(p.counter, 1) : 0;  // (no plan: no workspace write)
+                // (no plan: no workspace write)
+                const int idx = n_units <= 0 ? 0 : k == 0 ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(p.counter, 1);
                 UnitInfo u;
                 u.valid = idx < n_units;
                 if (u.valid) {
-                    const int4 rec = p.units[idx];
+                    const int4 rec = k == 0 ? first_rec : p.units[idx];
                     const int pair = rec.x / p.G;
                     u.g = rec.x - pair * p.G;
                     u.d = pair / p.B;
