@@ -32,7 +32,8 @@ uint64_t wait_limit_ns() {
     return kWaitLimitNs;
 }
 
-// [P1] 4.1 layer assignment (restated here for the library; see dcp_layer_range).
+// Layer assignment of "Serving Macaron-V1 at Scale: Page-Level 2D KV Resharding", 4.1 (restated
+// here for the library; see dcp_layer_range).
 void layer_range(int n_layers, int n_cp, int r, int *s, int *e) {
     const int base = n_layers / n_cp, extra = n_layers % n_cp;
     *s = r * base + (r < extra ? r : extra);

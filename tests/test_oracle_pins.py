@@ -5,6 +5,10 @@ on the pages (tests/golden/), a closed form, an invariant the pages state, a spe
 that reduces to a library routine (torch dtype casts, scipy softmax / logsumexp), or brute
 force on tiny inputs.  Together they are chosen so that a dropped term, a wrong sign or
 index, a transposed operand, an off-by-one mask or a wrong log base fails at least one.
+
+Citations: [P1] "Serving Macaron-V1 at Scale: Page-Level 2D KV Resharding" (Mind Lab), by
+section; [P2] "SGLang's path" (serving-k3, module 05), its paragraph on decode context
+parallelism.
 """
 import itertools
 import math
