@@ -67,6 +67,21 @@ def random_q(b: int, t: int, h: int, gen: torch.Generator, device) -> torch.Tens
     return q
 
 
+def check_page_table(req_page_ptr: torch.Tensor, dst_vpages: torch.Tensor) -> None:
+    """Checks a destination page table against the contract the library leaves to its caller:
+    CSR offsets non-decreasing from 0 to the table's length, and no page value twice (two
+    entries with one value would write, and read, the same pool slot).  Values outside the pools
+    are not checked here: the library flags those on the device.  Raises ValueError."""
+    ptr = req_page_ptr.detach().to("cpu", torch.int64)
+    vp = dst_vpages.detach().to("cpu", torch.int64)
+    if ptr.numel() < 1 or int(ptr[0]) != 0 or int(ptr[-1]) != vp.numel():
+        raise ValueError("req_page_ptr must run from 0 to the number of page entries")
+    if ptr.numel() > 1 and bool((ptr[1:] < ptr[:-1]).any()):
+        raise ValueError("req_page_ptr must be non-decreasing")
+    if vp.numel() and torch.unique(vp).numel() != vp.numel():
+        raise ValueError("a destination page value appears more than once in the table")
+
+
 def page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Generator, with_slots: bool = False):
     """Round-robin ownership with seeded random slots.  Returns (req_page_ptr, dst_vpages), and
     with ``with_slots`` also the owner rank and pool slot the generator chose for every entry
@@ -97,6 +112,7 @@ def page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Generator, 
             slots_of[k:k + p][sel] = slots
         k += p
     out = (torch.tensor(ptr, dtype=torch.int64), vp.to(torch.int32))
+    check_page_table(*out)
     return out + (owners, slots_of) if with_slots else out
 
 
@@ -122,6 +138,7 @@ def token_page_table(seq_lens, n_dcp: int, slots_per_rank: int, gen: torch.Gener
                 slots_of.append(slot)
         ptr.append(ptr[-1] + p * n_ranks)
     out = (torch.tensor(ptr, dtype=torch.int64), torch.tensor(vp, dtype=torch.int32))
+    check_page_table(*out)
     if with_slots:
         out += (torch.tensor(owners, dtype=torch.int64), torch.tensor(slots_of, dtype=torch.int64))
     return out
