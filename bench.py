@@ -411,7 +411,8 @@ def oracle_sample(wl, max_seconds: float = 20.0):
     """Times the float64 oracle on a bounded sample of the workload: request by request, the
     reshard of the request's pages (every layer), then for layer 0 the per-rank partial
     attention and merge of a subset of the request's query rows, until ~max_seconds.
-    Returns GB/s over the sample's share of the step's algorithmic bytes."""
+    Returns (GB/s over the sample's share of the step's algorithmic bytes, a description, seconds,
+    threads, seconds per stage)."""
     import numpy as np
 
     import oracle
@@ -428,6 +429,7 @@ def oracle_sample(wl, max_seconds: float = 20.0):
     step_rows = wl.B * rows_per_req * wl.L
     attn_merge = wl.bytes["attn"] + wl.bytes["merge"]
     done_bytes, t_total, n_req, n_rows = 0.0, 0.0, 0, 0
+    t_stage = {"reshard": 0.0, "attention": 0.0, "merge": 0.0}
     # request by request, cycling through the workload's requests until the time budget is spent
     while t_total < max_seconds and n_req < 64 * wl.B:
         b = n_req % wl.B
@@ -441,14 +443,20 @@ def oracle_sample(wl, max_seconds: float = 20.0):
         t0 = time.perf_counter()
         oracle.reshard(sub_ptr, src_pages[p0:p1], vp[p0:p1], rc.page_bytes, wl.L, src, rc.src_pool_pages, wl.N,
                        dst, rc.dst_slots)
+        t1 = time.perf_counter()
         esz = 2 if wl.dtype == "bf16" else 1
         pools = [d.reshape(wl.L, rc.dst_slots * 64 * 576 * esz)[0].view(np.uint16 if esz == 2 else np.uint8)
                  .reshape(rc.dst_slots, 64, 576) for d in dst]
         parts = [oracle.attention(qb[b:b + 1], np.array([wl.lens[b]], np.int32), sub_ptr, vp[p0:p1], pools,
                                   dt, wl.kv_scale, wl.scale, wl.N, rank=d, rows=rows, q_len=wl.T, num_heads=wl.H)
                  for d in range(wl.N)]
+        t2 = time.perf_counter()
         oracle.lse_merge(np.stack([p[0] for p in parts]), np.stack([p[1] for p in parts]))
-        t_total += time.perf_counter() - t0
+        t3 = time.perf_counter()
+        t_stage["reshard"] += t1 - t0
+        t_stage["attention"] += t2 - t1  # (the pools' views between the two are free)
+        t_stage["merge"] += t3 - t2
+        t_total += t3 - t0
         done_bytes += wl.bytes["reshard"] * (p1 - p0) / pages_total + attn_merge * len(rows) / step_rows
         n_req += 1
         n_rows += len(rows)
@@ -457,7 +465,7 @@ def oracle_sample(wl, max_seconds: float = 20.0):
               if n_req >= wl.B else f"{n_req} of {wl.B} requests")
     desc = (f"{passes}: each request's reshard ({wl.L} layers) + layer-0 partial attention over {wl.N} ranks and "
             f"merge for {n_rows} of {n_req * rows_per_req} query rows; {t_total:.1f} s")
-    return gbs, desc, t_total, oracle.num_threads()
+    return gbs, desc, t_total, oracle.num_threads(), t_stage
 
 
 # ------------------------------------------------------------------------------- main
@@ -467,12 +475,12 @@ def run_reference(args):
         return
     dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
     wl = Workload(args.config, dev, oracle_only=True)
-    vals, secs, desc, threads = [], [], "", 1
+    vals, secs, desc, threads, stages = [], [], "", 1, {}
     # the oracle has no warm state: warm-up steps are not run; the whole run stays near two
     # minutes of host time however many steps are asked for
     per_step = min(args.ref_seconds, max(2.0, 120.0 / max(args.steps, 1)))
     for _ in range(args.steps):
-        gbs, desc, t, threads = oracle_sample(wl, max_seconds=per_step)
+        gbs, desc, t, threads, stages = oracle_sample(wl, max_seconds=per_step)
         vals.append(gbs)
         secs.append(t)
     v = statistics.median(vals)
@@ -481,7 +489,8 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(wl, world),
-        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": v, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
+                         "stage_seconds": stages},
         "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -680,8 +689,17 @@ def run_ours(args):
                 "algorithmic_bytes": wl.stage_bytes[dom]}
     cpu = None
     if not args.no_cpu_baseline:
-        gbs, desc, secs, threads = oracle_sample(wl, max_seconds=args.ref_seconds)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
+        gbs, desc, secs, threads, t_stage = oracle_sample(wl, max_seconds=args.ref_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc,
+               "stage_seconds": t_stage}
+        if wl.name.startswith(("tiny", "batch")):  # the small workloads: one core as well
+            import oracle
+            oracle.set_num_threads(1)
+            try:
+                g1, d1, _, _, _ = oracle_sample(wl, max_seconds=min(5.0, args.ref_seconds))
+            finally:
+                oracle.set_num_threads(threads)
+            cpu["single_core"] = {"value": g1, "unit": "GB/s", "cores": 1, "sample": d1}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",

@@ -57,6 +57,7 @@ def _load():
             lib = ctypes.CDLL(build())
             i32, i64, dbl, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
             lib.dcpo_num_threads.restype = i32
+            lib.dcpo_set_num_threads.argtypes = [i32]
             lib.dcpo_layer_range.argtypes = [i32, i32, i32, vp, vp]
             lib.dcpo_filter_indices.argtypes = [vp, i64, i32, i32, vp]
             lib.dcpo_filter_indices.restype = i64
@@ -102,6 +103,11 @@ def _c(a, dtype) -> np.ndarray:
 def num_threads() -> int:
     """OpenMP threads the oracle's parallel loops use."""
     return int(_load().dcpo_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the oracle's parallel loops from now on (n < 1: one per processor)."""
+    _load().dcpo_set_num_threads(int(n))
 
 
 def layer_range(n_layers: int, n_cp: int, r: int) -> tuple[int, int]:

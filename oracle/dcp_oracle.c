@@ -41,6 +41,15 @@ int dcpo_num_threads(void) {
 #endif
 }
 
+/* Threads for the parallel loops that follow (n < 1: one per processor).  Timing only. */
+void dcpo_set_num_threads(int n) {
+#ifdef _OPENMP
+    omp_set_num_threads(n > 0 ? n : omp_get_num_procs());
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------------------ */
 /* [P1] 4.1 "Layer Assignment", layer-range equation: contiguous partition of L layers    */
 /* over N_cp ranks with base = floor(L / N_cp) and extra = L mod N_cp; rank r owns         */

@@ -25,6 +25,8 @@ def test_reference_arm_runs_the_oracle_on_the_host():
     assert line["value"] > 0 and line["unit"] == "GB/s" and line["higher_is_better"] is True
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["cpu_baseline"]["value"] == line["value"]
+    st = line["cpu_baseline"]["stage_seconds"]
+    assert set(st) == {"reshard", "attention", "merge"} and all(v >= 0 for v in st.values())
     assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert line["config"]["workload"].startswith("tiny-")
     assert {"bytes_per_step", "parallelism", "l2"} <= set(line["config"])
