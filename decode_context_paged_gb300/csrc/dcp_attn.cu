@@ -12,6 +12,8 @@
 //    request, chunk, query group), a query group being one new token and up to 64 heads.
 //    Units are ordered by size (largest first) with the groups of one chunk adjacent, and
 //    persistent CTAs (one per SM) take them from an atomic counter (CTA i starts with unit i).
+//    When the queue's last round would leave SMs idle, the plan cuts that round's chunks into
+//    balanced pieces (merged like chunks; deterministic, so results are reproducible).
 //  * Tokens are the MMA's M dimension (128 = two pages), query rows its N.  Per tile
 //    tcgen05 computes S^T[128 x n] = K_tile * Q^T into TMEM, the softmax warps turn it into
 //    P^T in shared memory, and tcgen05 accumulates O^T[512 x 64] += V_tile^T * P^T in TMEM.
