@@ -289,10 +289,11 @@ int dcp_partial_decode_attn(int num_requests, int q_len, int num_heads, const vo
  * order; all-empty rows give O = 0, LSE = -inf):
  *   o_out   fp32 [num_requests][q_len][num_heads][512]
  *   lse_out fp32 [num_requests][q_len][num_heads]
- * The merge runs in the launches that follow the attention kernel, while the partials are
- * still in L2: when no (rank, request) segment was split into chunks, the launch that would
- * combine chunk partials merges the ranks instead and the last launch exits at once; else the
- * chunks are combined first and the last launch merges.  The pages' deployment has one GPU
+ * The merge runs in the two launches that follow the attention kernel, while the partials are
+ * still in L2: the first combines the pieces of the (rank, request) segments the plan split
+ * (chunks of long segments, pieces of the queue's last round) and merges over the ranks the
+ * rows of every request none of whose segments was split; the second merges the rows of the
+ * other requests (it exits at once when nothing was split).  The pages' deployment has one GPU
  * per rank and an all-gather before the merge; on one GPU the gather is a read of the other
  * ranks' partials.
  *   workspace: >= dcp_partial_decode_attn_workspace_size(...) bytes, 256-byte aligned.
