@@ -1343,9 +1343,48 @@ __device__ void plan_build_units(int B, int N, int G, int only_rank, int tpc, in
     }
     __syncthreads();
     const int q = q_cut, ts = tail_start, uc = u_c, sb = s_b;
+    if (q == 0) {  // no cut: the partial slots first, then every unit with its final slot
+        long long running = 0;
+        for (int base = 0; base < n_pair; base += blockDim.x) {
+            const int pr = base + tid;
+            const int chunks = pr < n_pair ? pair_chunks[pr] : 0;
+            long long tot;
+            const long long off = block_exclusive_scan(chunks > 1 ? (long long)chunks * G : 0, scratch, &tot);
+            if (pr < n_pair) {
+                pair_part[pr] = chunks > 1 ? (int)(running + off) : -1;
+                if (chunks > 1) multi_list[atomicAdd(&n_multi, 1)] = pr;
+            }
+            running += tot;
+        }
+        __syncthreads();
+        for (int pr = tid; pr < n_pair; pr += blockDim.x) {
+            if (!active(pr)) continue;
+            const int cnt = counts[pr];
+            const int tiles = (cnt + 1) >> 1;
+            const int chunks = n_chunks(tiles);
+            for (int c = 0; c < chunks; ++c) {
+                const int pos = atomicAdd(&hist[chunk_size(tiles, c)], 1);
+                const int page_begin = c * 2 * tpc;
+                const int n_pages = max(0, min(2 * tpc, cnt - page_begin));
+                for (int g = 0; g < G; ++g)
+                    units[(long long)pos * G + g] =
+                        make_int4(pr * G + g, page_begin, n_pages, chunks > 1 ? pair_part[pr] + c * G + g : -1);
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            ctrl[0] = uc * G;
+            ctrl[1] = 0;
+            ctrl[2] = n_multi;
+            ctrl[3] = kPlanMagic;
+            *reinterpret_cast<unsigned long long *>(ctrl + 4) = key;
+            *reinterpret_cast<long long *>(ctrl + 6) = (long long)req_page_ptr[B];
+        }
+        return;
+    }
     // (request, rank, chunk) rank of each pair's first chunk of size sb among all chunks of that
     // size (kept in pair_part until the partial slots are assigned)
-    if (q > 0) {
+    {
         long long running = 0;
         for (int base = 0; base < n_pair; base += blockDim.x) {
             const int idx = base + tid;  // request-major
