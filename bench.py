@@ -57,9 +57,9 @@ NCU_TRAFFIC = {
     ("reshard_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("26b6b9b40d4d64dd", 552448000),
     ("reshard_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("26b6b9b40d4d64dd", 5236858368),
     ("reshard_kernel", "e2e-64x463936-h64-q1-e4m3-dcp8-L8-cp4"): ("26b6b9b40d4d64dd", 44745598653),
-    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("a8f513edd53163b9", 325701888),
-    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("a8f513edd53163b9", 2791083776),
-    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("a8f513edd53163b9", 2528831488),
+    ("attn_kernel", "batch-32x8192-h64-q1-bf16-dcp8"): ("b5795b2a10f59e5a", 325355776),
+    ("attn_kernel", "agent-48x100000-h64-q1-e4m3-dcp8"): ("b5795b2a10f59e5a", 2790926848),
+    ("attn_kernel", "long-4x1048576-h64-q4-e4m3-dcp8"): ("b5795b2a10f59e5a", 2528633856),
 }
 
 
