@@ -33,7 +33,8 @@
  *     buffer; the library allocates nothing and keeps no state between calls, except
  *     dcp_partial_decode_attn_static's fixed scratch array (see there).  Outputs must not
  *     alias inputs.
- *   - Calls are asynchronous on `stream` (NULL = the legacy default stream).  Argument and
+ *   - Calls are asynchronous on `stream` (NULL = the legacy default stream; the diagnostic
+ *     dcp_attn_plan_info alone synchronises it to read the plan back).  Argument and
  *     shape errors are detected on the host before anything is launched and return a
  *     negative dcp_status.  Problems only visible on the device (a page value or index
  *     outside its pool, a pipeline wait that ran past its time limit) are OR-ed into the
