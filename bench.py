@@ -663,6 +663,10 @@ def run_ours(args):
         return
     hbm, bf16, bf16_sus, peak_kind = peaks()
     plan_ms = stage_ms.pop("plan", None)  # on the side stream, overlapped with the reshard
+    plan_info = None
+    if plan_ms is not None and wl.layout != "token":  # the plan's queue, read back after the timed passes
+        torch.cuda.synchronize()
+        plan_info = dcp.attn_plan_info((wl.B, wl.T, wl.H), wl.rc.dst_vpages.numel(), wl.layer_pools[0], wl.ws)
     stage_gbs = {k: wl.stage_bytes[k] / (stage_ms[k] * 1e-3) / 1e9 for k in stage_ms}
     attn_tflops = wl.flops_attn / (stage_ms["attn"] * 1e-3) / 1e12
     dom = max(stage_ms, key=stage_ms.get)
@@ -726,7 +730,9 @@ def run_ours(args):
                      "includes_merge": wl.fused},
             **({} if wl.fused else {"merge": {"ms": stage_ms["merge"], "GB/s": stage_gbs["merge"],
                                               "frac_hbm": stage_gbs["merge"] / hbm}}),
-            **({"plan": {"ms": plan_ms, "stream": "side, overlapped with the reshard; once per step"}}
+            **({"plan": {"ms": plan_ms, "stream": "side, overlapped with the reshard; once per step",
+                         **({"units": plan_info["units"], "split_pairs": plan_info["split_pairs"],
+                             "tiles_per_chunk": plan_info["tiles_per_chunk"]} if plan_info else {})}}
                if plan_ms is not None else {}),
             "pass": {"steps": args.steps, "ms_per_step": staged_ms_step,
                      "note": "second timed pass with CUDA events around each stage"},

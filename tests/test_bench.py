@@ -62,7 +62,7 @@ def test_cuda_arm_line(cuda_device):
 def _rank_main(rank, world, port, q):
     import os
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
-                      LOCAL_RANK=str(rank))
+                      LOCAL_RANK=str(rank), CUDA_VISIBLE_DEVICES="")  # gloo CPU ranks on any machine
     import sys
     sys.path.insert(0, ROOT)
     import bench
