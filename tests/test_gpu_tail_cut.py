@@ -27,40 +27,47 @@ def _pair_tiles(case):
 
 
 def _expected(case, tpc, sms):
-    """(units, pairs with several pieces) by the rule the plan applies (host restatement)."""
+    """(units, pairs with several pieces, whether the tail is cut) by the rule the plan applies (host restatement): chunks
+    of tpc tiles; the queue in (size descending, request, rank, chunk) order; if its last round
+    is partly filled, the chunks from that round's first position on laid end to end and cut at
+    the multiples of q = their tiles x G / SMs, when that pays and fits the workspace."""
     G = case.T * ((case.H + 63) // 64)
-    chunks = [1 if t == 0 else -(-t // tpc) for t in _pair_tiles(case)]
-    sizes = []
-    for t, c in zip(_pair_tiles(case), chunks):
-        sizes += [max(0, min(tpc, t - k * tpc)) for k in range(c)]
-    multi_before = sum(1 for c in chunks if c > 1)
-    part_before = sum(c * G for c in chunks if c > 1)
+    B, N = case.B, case.n_dcp
+    tiles = _pair_tiles(case)
+    chunks, items = {}, []
+    for d in range(N):
+        for b in range(B):
+            pr = d * B + b
+            t = tiles[pr]
+            chunks[pr] = 1 if t == 0 else -(-t // tpc)
+            items += [(max(0, min(tpc, t - c * tpc)), (b * N + d, c), pr) for c in range(chunks[pr])]
+    split = {pr for pr, ch in chunks.items() if ch > 1}
+    part_before = sum(ch * G for ch in chunks.values() if ch > 1)
     n_pages = int(case.req_page_ptr[-1])
-    n_pair = case.n_dcp * case.B
-    max_partials = (G * (n_pages + n_pair)) // tpc + G
-    max_units = n_pair * G + max_partials
-    u_c = len(sizes)
+    max_partials = (G * (n_pages + N * B)) // tpc + G
+    max_units = N * B * G + max_partials
+    u_c = len(items)
     total = u_c * G
     full = total // sms
     if full < 1 or total % sms == 0:
-        return total, multi_before
+        return total, len(split), False
     ts = -(-(full * sms) // G)
-    tail = sorted(sizes, reverse=True)[ts:]
-    s_tail, smax = sum(tail), (tail[0] if tail else 0)
+    tail = sorted(items, key=lambda x: (-x[0], x[1]))[ts:]
+    s_tail, smax = sum(x[0] for x in tail), (tail[0][0] if tail else -1)
     q = -(-(s_tail * G) // sms)
     cuts = s_tail // q if q else 0
     pays = q >= 8 and 4 * smax > 5 * q + 16
     fits = (u_c - ts <= 512 and total + cuts * G <= max_units and part_before + (cuts + u_c - ts) * G <= max_partials)
     if not (pays and fits):
-        return total, multi_before
-    extra, cut_chunks, o = 0, 0, 0
-    for sz in tail:
+        return total, len(split), False
+    extra, o = 0, 0
+    for sz, _, pr in tail:
         k = (o + sz - 1) // q - o // q + 1 if sz > 0 else 1
+        if k > 1:
+            split.add(pr)
         extra += k - 1
-        cut_chunks += k > 1
         o += sz
-    assert multi_before == 0, "the cases below have one chunk per pair"
-    return (u_c + extra) * G, cut_chunks
+    return (u_c + extra) * G, len(split), True
 
 
 def _plan(case):
@@ -96,8 +103,8 @@ def test_tail_cut_counts_and_parity(cuda_device, T):
     sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
     case = _cut_case(cuda_device, sms, T)
     ws, info = _plan(case)
-    units, split = _expected(case, info["tiles_per_chunk"], sms)
-    assert split > 0, "the case is built so that the rule cuts"
+    units, split, cut = _expected(case, info["tiles_per_chunk"], sms)
+    assert cut and split > 0, "the case is built so that the rule cuts"
     assert (info["units"], info["split_pairs"]) == (units, split)
     # planned run and one-call run: partials of every rank and the merged output vs the oracle
     err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
@@ -127,6 +134,44 @@ def test_tail_cut_rule_on_the_workloads(cuda_device, name):
     sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
     case = di.agent_case(cuda_device) if name == "agent" else di.batch_case(cuda_device)
     _, info = _plan(case)
-    assert (info["units"], info["split_pairs"]) == _expected(case, info["tiles_per_chunk"], sms)
+    assert (info["units"], info["split_pairs"]) == _expected(case, info["tiles_per_chunk"], sms)[:2]
     if sms == 152:
         assert (info["split_pairs"] > 0) == (name == "agent")
+
+
+# Seeded mixed lengths (multiples of 64 tokens), chosen so that on a 152-SM GB300 some segments
+# are already chunked and the last round is cut: the boundary size's chunks are then taken by
+# their (request, rank, chunk) rank and pieces join pairs that already hold several chunks.
+MIXED = [(1, 24, (300, 1700), 2), (25, 40, (300, 1700), 1)]
+
+
+@pytest.mark.parametrize("seed,B,pages,T", MIXED, ids=[f"seed{m[0]}-q{m[3]}" for m in MIXED])
+def test_tail_cut_with_mixed_lengths_and_chunked_segments(cuda_device, seed, B, pages, T):
+    import random
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    rng = random.Random(seed)
+    lens = [64 * rng.randint(*pages) for _ in range(B)]
+    case = di.attention_case(lens, H=64, T=T, n_dcp=8, dtype="e4m3", slots_per_rank=None, seed=seed,
+                             device=cuda_device, name=f"mixed-{seed}")
+    ws, info = _plan(case)
+    units, split, cut = _expected(case, info["tiles_per_chunk"], sms)
+    assert (info["units"], info["split_pairs"]) == (units, split)
+    if sms == 152:  # the premise of the case: segments already chunked, and a cut tail
+        tiles = _pair_tiles(case)
+        assert cut and max(tiles) > info["tiles_per_chunk"]
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    args = (case.q, case.seq_lens, case.req_page_ptr, case.dst_vpages, case.pools, case.softmax_scale, case.kv_scale)
+    om, lm, o, l = dcp.decode_attn_merged(*args, workspace=ws, dev_error=err, planned=True)
+    o1, l1 = dcp.partial_decode_attn(*args, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(o, o1) and torch.equal(l, l1)
+    o, l, om, lm = (t.cpu().numpy() for t in (o, l, om, lm))
+    rows = np.array([(b * case.T + t) * case.H + h for b in range(case.B) for t in range(case.T)
+                     for h in ((7 * b) % 64, 63 - (5 * b) % 64)], np.int64)
+    qb, pools = q_bits(case), pool_bytes(case)
+    for d in range(case.n_dcp):
+        ro, rl = oracle_attention(case, rank=d, rows=rows, qb=qb, pools=pools)
+        compare(o[d].reshape(-1, 512)[rows], l[d].reshape(-1)[rows], ro, rl, f"{case.name} rank {d}")
+    ro, rl = oracle_attention(case, rows=rows, qb=qb, pools=pools)
+    compare(om.reshape(-1, 512)[rows], lm.reshape(-1)[rows], ro, rl, f"{case.name} merged")
