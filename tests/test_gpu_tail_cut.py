@@ -142,17 +142,17 @@ def test_tail_cut_rule_on_the_workloads(cuda_device, name):
 # Seeded mixed lengths (multiples of 64 tokens), chosen so that on a 152-SM GB300 some segments
 # are already chunked and the last round is cut: the boundary size's chunks are then taken by
 # their (request, rank, chunk) rank and pieces join pairs that already hold several chunks.
-MIXED = [(1, 24, (300, 1700), 2), (25, 40, (300, 1700), 1)]
+MIXED = [(1, 24, (300, 1700), 2, "e4m3"), (25, 40, (300, 1700), 1, "e4m3"), (25, 40, (300, 1700), 1, "bf16")]
 
 
-@pytest.mark.parametrize("seed,B,pages,T", MIXED, ids=[f"seed{m[0]}-q{m[3]}" for m in MIXED])
-def test_tail_cut_with_mixed_lengths_and_chunked_segments(cuda_device, seed, B, pages, T):
+@pytest.mark.parametrize("seed,B,pages,T,dtype", MIXED, ids=[f"seed{m[0]}-q{m[3]}-{m[4]}" for m in MIXED])
+def test_tail_cut_with_mixed_lengths_and_chunked_segments(cuda_device, seed, B, pages, T, dtype):
     import random
     sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
     rng = random.Random(seed)
     lens = [64 * rng.randint(*pages) for _ in range(B)]
-    case = di.attention_case(lens, H=64, T=T, n_dcp=8, dtype="e4m3", slots_per_rank=None, seed=seed,
-                             device=cuda_device, name=f"mixed-{seed}")
+    case = di.attention_case(lens, H=64, T=T, n_dcp=8, dtype=dtype, slots_per_rank=None, seed=seed,
+                             device=cuda_device, name=f"mixed-{seed}-{dtype}")
     ws, info = _plan(case)
     units, split, cut = _expected(case, info["tiles_per_chunk"], sms)
     assert (info["units"], info["split_pairs"]) == (units, split)
@@ -169,6 +169,34 @@ def test_tail_cut_with_mixed_lengths_and_chunked_segments(cuda_device, seed, B, 
     o, l, om, lm = (t.cpu().numpy() for t in (o, l, om, lm))
     rows = np.array([(b * case.T + t) * case.H + h for b in range(case.B) for t in range(case.T)
                      for h in ((7 * b) % 64, 63 - (5 * b) % 64)], np.int64)
+    qb, pools = q_bits(case), pool_bytes(case)
+    for d in range(case.n_dcp):
+        ro, rl = oracle_attention(case, rank=d, rows=rows, qb=qb, pools=pools)
+        compare(o[d].reshape(-1, 512)[rows], l[d].reshape(-1)[rows], ro, rl, f"{case.name} rank {d}")
+    ro, rl = oracle_attention(case, rows=rows, qb=qb, pools=pools)
+    compare(om.reshape(-1, 512)[rows], lm.reshape(-1)[rows], ro, rl, f"{case.name} merged")
+
+
+def test_tail_cut_on_the_token_interleaved_layout(cuda_device):
+    """The token-interleaved layout's one-call attention makes the same plan (its table holds
+    rank d's local page jj at entry jj N + d): the cut applies alike, and the partials of every
+    rank and their merge match the oracle over that layout."""
+    sms = torch.cuda.get_device_properties(cuda_device).multi_processor_count
+    B = -(-sms * 10 // 48) + 8
+    case = di.token_attention_case([81_920] * B, H=64, T=1, n_dcp=8, dtype="e4m3", seed=47, device=cuda_device,
+                                   name=f"tail-cut-tokens-{B}x81920")
+    ws = dcp.alloc_workspace(case.B, case.T, case.H, case.n_dcp, case.dst_vpages.numel(), cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    o, l = dcp.partial_decode_attn(case.q, case.seq_lens, case.req_page_ptr, case.dst_vpages, case.pools,
+                                   case.softmax_scale, case.kv_scale, workspace=ws, dev_error=err, layout="token")
+    info = dcp.attn_plan_info((case.B, case.T, case.H), case.dst_vpages.numel(), case.pools, ws)
+    om, lm = dcp.lse_merge(o, l)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0 and info["valid"]
+    units, split, cut = _expected(case, info["tiles_per_chunk"], sms)
+    assert (info["units"], info["split_pairs"]) == (units, split) and cut
+    o, l, om, lm = (t.cpu().numpy() for t in (o, l, om, lm))
+    rows = np.array([b * case.H + h for b in range(case.B) for h in ((3 * b) % 64, 63 - b % 64)], np.int64)
     qb, pools = q_bits(case), pool_bytes(case)
     for d in range(case.n_dcp):
         ro, rl = oracle_attention(case, rank=d, rows=rows, qb=qb, pools=pools)
